@@ -1,0 +1,405 @@
+#!/usr/bin/env python3
+"""Benchmark of the warp-specialized pipeline library on one GB300.
+
+Default step: one bf16 GEMM + bias + ReLU, M = N = K = 8192 (A, B ~ N(0,1)/sqrt(K)
+cast to bf16, bias ~ N(0, 0.1), seed 3), 4-stage ring, persistent CTAs, 128x256x64
+tiles -- the workload the TFLOP/s half of the metric is quoted on.  The same run
+also times the bandwidth half: the TMA staged copy of an fp32 [16384, 4096]
+tensor (256 MiB, U[-1e3, 1e3], seed 1) with 128x64 tiles, reported under
+"staged_copy" with its own roofline.
+
+Prints ONE JSON line.  `--impl reference` times the CPU oracle instead (the
+plain binary64 triple loop on the host cores, on a bounded sample of rows).
+Under torchrun each rank runs its own replica of the workload (weak scaling);
+timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TFLOP/s of ReLU(A·B+bias) and GB/s of TMA staged copy, as % of GB300 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_FILES = ["gbr_ptx.cuh", "gbr_common.cuh", "gbr_internal.h", "gemm_umma.cu",
+                "staged_copy.cu", "gemm_ffma.cu", "transpose.cu"]
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "mbarrier_gemm_pipelines_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source
+    has not changed since it was captured (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel_key)
+    if not rec:
+        return None
+    if rec.get("source_hash") != kernel_source_hash(rec.get("files", KERNEL_FILES)):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.out = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "") else None,
+                             "hw": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
+                             "sw_power": parts[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["power"] is None or r["power"] > 300] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def dist_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def emit(obj):
+    print(json.dumps(obj), flush=True)
+
+
+# ----------------------------------------------------------------------------- CPU baseline
+
+def cpu_gemm_sample(A, B, bias, target_s=15.0):
+    """Times the binary64 oracle on the first rows of the product, as many as fit
+    in about target_s seconds (calibrated on one row per thread).  Returns (TFLOP/s, rows, s)."""
+    import oracle
+    A32, B32, b32 = A.float(), B.float(), bias.float()
+    K, N = B32.shape
+    nthr = oracle.max_threads()
+    cal = max(4, nthr)
+    for _ in range(2):                      # the first pass pages B in and starts the threads
+        t0 = time.perf_counter()
+        oracle.gemm_bias_relu(A32[:cal], B32, b32)
+        dt = max(time.perf_counter() - t0, 1e-6)
+    rows = int(max(cal, min(A32.shape[0], cal * target_s / dt)))
+    t0 = time.perf_counter()
+    oracle.gemm_bias_relu(A32[:rows], B32, b32)
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * N * K / dt / 1e12, rows, dt
+
+
+def cpu_copy_sample(src, target_s=5.0):
+    import numpy as np
+    import oracle
+    x = src.numpy()
+    y = np.empty_like(x)
+    n = oracle.max_threads()
+    reps, t_total = 0, 0.0
+    while t_total < target_s and reps < 200:
+        t0 = time.perf_counter()
+        oracle.copy_into(x, y, nthreads=n)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return 2.0 * x.nbytes * reps / t_total / 1e9, reps, t_total
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def gemm_flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+def time_launches(fn, steps, stream):
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def measure_copy(gbr, peaks, stages=4, steps=40, warmup=5):
+    import torch
+    from mbarrier_gemm_pipelines_gb300 import inputs
+    src = inputs.workload("copy").cuda()
+    dst = torch.empty_like(src)
+    stream = torch.cuda.current_stream()
+    out = {}
+    for S in (2, 4, 7):
+        def run():
+            gbr.staged_copy(src, dst, tile=(128, 64), stages=S)
+        for _ in range(warmup):
+            run()
+        t = time_launches(run, steps, stream)
+        gbr.check_device()
+        gbs = 2.0 * src.numel() * 4 * steps / t / 1e9
+        out[S] = gbs
+    best_S = max(out, key=out.get)
+    achieved = out[stages]
+    return {
+        "workload": "TMA staged copy fp32 [16384, 4096] (256 MiB) U[-1e3,1e3] seed 1, tiles 128x64",
+        "stages": stages, "value": round(achieved, 1), "unit": "GB/s",
+        "by_stages": {str(k): round(v, 1) for k, v in out.items()}, "best_stages": best_S,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": recorded_traffic("staged_copy"),
+                     "algorithmic_bytes_per_launch": 2 * src.numel() * 4},
+    }
+
+
+def run_ours(args):
+    import torch
+    import mbarrier_gemm_pipelines_gb300 as gbr
+    from mbarrier_gemm_pipelines_gb300 import inputs
+
+    world, rank, local = dist_setup()
+    gbr.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+
+    M = N = K = 8192
+    S = args.stages
+    A, B, bias = inputs.workload("gemm_bf16")
+    dA, dB, dbias = A.to(dev), B.to(dev), bias.to(dev)
+    dC = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gbr.gemm_bias_relu(dA, dB, dbias, dC, dtype="bf16", stages=S, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    gbr.check_device()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    dist_barrier(world)
+    launches0 = gbr.launch_count()
+    t = time_launches(step, args.steps, stream)
+    launches = gbr.launch_count() - launches0
+    dist_barrier(world)
+    clocks = sampler.stop()
+    gbr.check_device()
+    t = dist_max(t, world)
+
+    flops = gemm_flops(M, N, K)
+    value = flops * args.steps * world / t / 1e12
+    per_launch = t / args.steps
+    achieved = flops / per_launch / 1e12
+
+    # End to end through the public API: pinned host inputs -> device -> GEMM -> host.
+    hA, hB, hbias = A.pin_memory(), B.pin_memory(), bias.pin_memory()
+    hC = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        dbias.copy_(hbias, non_blocking=True)
+        gbr.gemm_bias_relu(dA, dB, dbias, dC, dtype="bf16", stages=S, stream=stream)
+        hC.copy_(dC, non_blocking=True)
+
+    e2e_step()
+    t_e2e = dist_max(time_launches(e2e_step, e2e_steps, stream), world)
+    h2d = hA.numel() * 2 + hB.numel() * 2 + hbias.numel() * 4
+    d2h = hC.numel() * 2
+
+    copy = measure_copy(gbr, peaks) if rank == 0 else None
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, rows, secs = cpu_gemm_sample(A, B, bias, target_s=args.cpu_seconds)
+        import oracle
+        cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
+               "kind": "oracle",
+               "sample": "first %d of %d rows of the 8192^3 product (binary64 i-k-j loop, "
+                         "%.1f s)" % (rows, M, secs)}
+
+    if rank != 0:
+        return
+    peak_key = "bf16_tflops"
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "bf16 GEMM+bias+ReLU M=N=K=8192, A,B~N(0,1)/sqrt(K)->bf16, "
+                               "bias f32~N(0,0.1), seed 3; persistent 128x256x64 tiles, "
+                               "%d-stage TMA/mbarrier ring, tcgen05 MMA into TMEM" % S,
+                   "M": M, "N": N, "K": K, "stages": S,
+                   "l2": "inputs larger than L2 (A+B = 256 MiB > 129 MB); no flush",
+                   "parallelism": "replica per GPU" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peaks.get(peak_key, FALLBACK_PEAKS[peak_key]), "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks.get(peak_key, FALLBACK_PEAKS[peak_key]), 4),
+                     "traffic": recorded_traffic("gemm_umma_bf16"),
+                     "peak_source": "%s %s (burst cuBLAS bf16); sustained %s" % (
+                         peak_src, peak_key, peaks.get("bf16_tflops_sustained"))},
+        "e2e": {"value": round(flops * e2e_steps / t_e2e / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "steps": e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "staged_copy": copy,
+    }
+    emit(res)
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on the machine's host cores."""
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return
+    import oracle
+    from mbarrier_gemm_pipelines_gb300 import inputs
+    oracle.build()
+    A, B, bias = inputs.workload("gemm_bf16")
+    per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_gemm_sample(A, B, bias, target_s=per_step)
+    vals, rows_used, secs = [], 0, 0.0
+    for _ in range(args.steps):
+        v, rows, s = cpu_gemm_sample(A, B, bias, target_s=per_step)
+        vals.append(v)
+        rows_used += rows
+        secs += s
+    value = statistics.median(vals)
+    sample = ("per step: first ~%d of 8192 rows of the 8192^3 bf16 product, binary64 i-k-j loop"
+              % (rows_used // max(1, args.steps)))
+    res = {
+        "metric": METRIC, "impl": "reference", "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / max(1, args.steps) * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "bf16 GEMM+bias+ReLU M=N=K=8192 (oracle on a row sample)",
+                   "M": 8192, "N": 8192, "K": 8192},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
+                         "cores": oracle.max_threads(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    emit(res)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--stages", type=int, default=4)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

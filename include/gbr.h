@@ -1,0 +1,181 @@
+/*
+ * gbr.h -- C ABI of the warp-specialized TMA/mbarrier pipeline library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Two operators, both built as one producer role that streams tiles through
+ * an S-slot shared-memory ring guarded by per-slot "full" and "empty"
+ * mbarriers (slot = i % S, full wait parity = (i / S) & 1, empty wait parity =
+ * ((i / S) & 1) ^ 1), and consumer roles that work on full slots and release
+ * them:
+ *
+ *   gemm_bias_relu          C = ReLU(A * B + bias)
+ *   gemm_bias_relu_grouped  the same per expert segment (MoE-style), one launch
+ *   staged_copy             gmem -> smem -> gmem through the ring (TMA both ways)
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are contiguous, row-major, resident in device memory of the
+ *     current CUDA device, allocated and owned by the caller.  The library
+ *     never frees or retains them after the call's work has finished.
+ *   - `stream` is a cudaStream_t (a CUstream_st pointer); NULL is the legacy
+ *     default stream.  Every call is asynchronous on that stream.
+ *   - Return value: GBR_OK, or an error code for host-side validation or launch
+ *     failures, with a message available from gbr_last_error() on the calling
+ *     thread.  Nothing is launched when validation fails.
+ *   - Device-side failures (a pipeline wait that exceeded its time limit) are
+ *     reported by gbr_device_status(), which also clears them.
+ *   - Global addresses must be 16-byte aligned and every row pitch must be a
+ *     multiple of 16 bytes (the TMA rule): fp32 row lengths a multiple of 4,
+ *     bf16 row lengths a multiple of 8.  Otherwise GBR_ERR_ALIGN.
+ *   - The library keeps, per device, a 64-byte status block it allocates on
+ *     first use, plus cached device attributes.
+ */
+#ifndef GBR_H_
+#define GBR_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *gbr_stream_t;
+
+typedef enum {
+    GBR_F32_FFMA = 0, /* fp32 in/out, strict fp32 FMA on CUDA cores        */
+    GBR_F32_TF32 = 1, /* fp32 in/out, TF32 tensor-core multiply, fp32 acc   */
+    GBR_BF16 = 2      /* bf16 A/B/C, fp32 bias, fp32 accumulation in TMEM   */
+} gbr_dtype;
+
+typedef enum {
+    GBR_OK = 0,
+    GBR_ERR_INVALID = 1,     /* bad size, pointer, count or overlapping buffers */
+    GBR_ERR_UNSUPPORTED = 2, /* dtype/operator combination not built            */
+    GBR_ERR_ALIGN = 3,       /* address or row pitch violates the TMA rule       */
+    GBR_ERR_SMEM = 4,        /* stages outside [1, gbr_max_stages(...)]          */
+    GBR_ERR_CUDA = 5,        /* CUDA runtime/driver error (message has details)  */
+    GBR_ERR_TIMEOUT = 6      /* a device-side pipeline wait gave up              */
+} gbr_status;
+
+/*
+ * gemm_bias_relu -- C[m,n] = max(0, bias[n] + sum_k A[m,k] * B[k,n]).
+ *
+ * Defined by the SGEMM test bench of "pwwt.cn news/4436243", section 4.1
+ * (inputs A[M,K], B[K,N]; output A*B + bias followed by ReLU), computed by
+ * the warp-specialized ring of section 3.4 of the same page and of
+ * "gpu_warp_specialization" ("End-to-end flow").
+ *
+ *   A     [M, K] row-major; fp32 (GBR_F32_*) or bf16 (GBR_BF16).  Read only.
+ *   B     [K, N] row-major; same type as A.  Read only.
+ *   bias  [N] fp32.  Read only.
+ *   C     [M, N] row-major; fp32 (GBR_F32_*) or bf16 (GBR_BF16, rounded to
+ *         nearest even from the fp32 result).  Written; must not overlap the
+ *         inputs.
+ *   M, N, K  >= 0 and < 2^31.  M == 0 or N == 0: nothing to do.  K == 0:
+ *         C = max(0, bias) in every row.  A and B may be NULL when K == 0.
+ *   dtype gbr_dtype.
+ *   stages  ring depth S, 1 <= S <= gbr_max_stages(GBR_OP_GEMM, dtype, 0, 0)
+ *         (GBR_ERR_SMEM otherwise).  Tiles: FFMA 128x128x32 fp32;
+ *         tcgen05 128x256 with 128 bytes of K per stage (bf16 K=64, tf32 K=32).
+ *   stream  see above.
+ * Ragged M, N and K need no padding: TMA loads zero-fill outside the tensor
+ * and TMA stores drop rows/columns outside it.
+ */
+int gemm_bias_relu(const void *A, const void *B, const float *bias, void *C, int64_t M,
+                   int64_t N, int64_t K, int dtype, int stages, gbr_stream_t stream);
+
+/*
+ * gemm_bias_relu_grouped -- per expert e (0 <= e < num_groups):
+ *   C[r,n] = max(0, b[e,n] + sum_k X[r,k] * W[e,k,n]) for r in
+ *   [off_e, off_e + counts[e]), off_e = counts[0] + ... + counts[e-1].
+ *
+ * The mixture-of-experts operator that motivates "pwwt.cn news/4436243"
+ * (section 1.1), expressed as the same GEMM + bias + ReLU per expert and run
+ * as ONE persistent warp-specialized launch over all experts' tiles.
+ *
+ *   X     [T, K] rows already grouped by expert, T = sum(counts).  Read only.
+ *   W     [G, K, N] expert weights.  Read only.
+ *   bias  [G, N] fp32.  Read only.
+ *   C     [T, N] written row segment by row segment.
+ *   counts_host  HOST array of num_groups non-negative row counts (read
+ *         during the call only); a zero count gives the expert no tiles.
+ *   num_groups  1..32.
+ *   dtype GBR_BF16 (GBR_ERR_UNSUPPORTED for the others).
+ *   stages  as for gemm_bias_relu.
+ * Routing and permutation of tokens are the caller's.
+ */
+int gemm_bias_relu_grouped(const void *X, const void *W, const float *bias, void *C,
+                           const int32_t *counts_host, int num_groups, int64_t K, int64_t N,
+                           int dtype, int stages, gbr_stream_t stream);
+
+/*
+ * staged_copy -- dst = src, moved tile by tile gmem -> smem -> gmem by TMA.
+ *
+ * The double-buffered TMA load/store example of "Producer-Consumer Warp
+ * Specialization for TMA Operations" generalised to an S-slot ring: one
+ * lane loads tile i into slot i % S and one lane stores it back out; the
+ * slot is handed back once the store has finished reading shared memory.
+ *
+ *   src, dst  [rows, cols] of 4-byte elements (fp32 or any 32-bit type; the
+ *         copy is bit-exact).  src read only; dst written; they must not overlap.
+ *   rows, cols  >= 0 and < 2^31; cols a multiple of 4.  Empty: nothing to do.
+ *   tile_rows  1..256; tile_cols 4..256, a multiple of 4 (16-byte rows).
+ *   stages  1 <= S <= gbr_max_stages(GBR_OP_COPY, 0, tile_rows, tile_cols),
+ *         i.e. S * tile_rows * tile_cols * 4 bytes must fit in one CTA's
+ *         shared memory (GBR_ERR_SMEM otherwise; at 128x64 fp32 S <= 7).
+ */
+int staged_copy(const void *src, void *dst, int64_t rows, int64_t cols, int tile_rows,
+                int tile_cols, int stages, gbr_stream_t stream);
+
+/*
+ * gbr_device_status -- synchronises `stream`, then reports and clears the
+ * current device's status block.  GBR_OK, GBR_ERR_TIMEOUT (a pipeline wait in
+ * a kernel exceeded its limit; the kernel raised its abort flag, let its own
+ * copies in flight finish, released its Tensor Memory and returned, so the
+ * context stays usable; the output of that call is undefined), or
+ * GBR_ERR_CUDA for a CUDA error seen while synchronising.
+ */
+int gbr_device_status(gbr_stream_t stream);
+
+/* Message of the last failing call on this thread ("" if none).  The pointer
+ * stays valid until the next library call on this thread. */
+const char *gbr_last_error(void);
+
+enum { GBR_OP_GEMM = 0, GBR_OP_COPY = 1 };
+
+/* Largest ring depth that fits the current device's per-CTA shared memory:
+ * op GBR_OP_GEMM uses `dtype`; GBR_OP_COPY uses tile_rows x tile_cols fp32.
+ * Returns a negative gbr_status on error. */
+int gbr_max_stages(int op, int dtype, int tile_rows, int tile_cols);
+
+/* Number of kernels this library has launched in this process. */
+long long gbr_launch_count(void);
+
+/* Number of SMs of the current device (negative gbr_status on error). */
+int gbr_sm_count(void);
+
+/* Per-wait time limit in nanoseconds for every pipeline wait; 0 restores the
+ * default (environment variable GBR_WAIT_TIMEOUT_NS, else 2 s). */
+int gbr_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Staged-copy tuning, process-wide.  store_lag: -1 auto, 0 (release a slot
+ * once its own store has read it) or 1 (release the previous slot after the
+ * next store is issued; needs stages >= 2).  ctas_per_sm: -1 auto (as many
+ * as shared memory allows), else 1..occupancy.
+ */
+int gbr_copy_tuning(int store_lag, int ctas_per_sm);
+
+/*
+ * Failure-detection self test: launches one CTA that waits, with the given
+ * limit, on an mbarrier phase nothing will complete.  The wait gives up, the
+ * kernel records a timeout and returns; gbr_device_status() then reports
+ * GBR_ERR_TIMEOUT.  No GPU fault or hang is involved.
+ */
+int gbr_selftest_wait_timeout(uint64_t timeout_ns, gbr_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBR_H_ */

@@ -1,0 +1,202 @@
+"""ctypes binding of ``libgbr.so`` (declared in ``include/gbr.h``).
+
+Argument marshalling only: every step of every operator runs in the CUDA
+kernels of the library.  There is no CPU or PyTorch fallback; if the library
+is missing or the tensors are not on a CUDA device the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+# gbr_dtype
+F32_FFMA, F32_TF32, BF16 = 0, 1, 2
+DTYPE_NAMES = {"ffma": F32_FFMA, "tf32": F32_TF32, "bf16": BF16}
+# gbr_status
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_ALIGN, ERR_SMEM, ERR_CUDA, ERR_TIMEOUT = range(7)
+STATUS_NAMES = {0: "GBR_OK", 1: "GBR_ERR_INVALID", 2: "GBR_ERR_UNSUPPORTED", 3: "GBR_ERR_ALIGN",
+                4: "GBR_ERR_SMEM", 5: "GBR_ERR_CUDA", 6: "GBR_ERR_TIMEOUT"}
+OP_GEMM, OP_COPY = 0, 1
+
+# Every function the header declares: name -> (restype, argtypes).
+_vp, _i64, _i32, _u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
+SIGNATURES = {
+    "gemm_bias_relu": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp]),
+    "gemm_bias_relu_grouped": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _i32, _vp]),
+    "staged_copy": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp]),
+    "gbr_device_status": (_i32, [_vp]),
+    "gbr_last_error": (ctypes.c_char_p, []),
+    "gbr_max_stages": (_i32, [_i32, _i32, _i32, _i32]),
+    "gbr_launch_count": (ctypes.c_longlong, []),
+    "gbr_sm_count": (_i32, []),
+    "gbr_set_wait_timeout_ns": (_i32, [_u64]),
+    "gbr_copy_tuning": (_i32, [_i32, _i32]),
+    "gbr_selftest_wait_timeout": (_i32, [_u64, _vp]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class GbrError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__("%s: %s" % (STATUS_NAMES.get(code, str(code)), msg))
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """Loads libgbr.so (it must have been built: ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError("libgbr.so is not built (%s); run __graft_entry__.build()" % path)
+            h = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(h, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = h
+        return _lib
+
+
+def last_error() -> str:
+    return (lib().gbr_last_error() or b"").decode()
+
+
+def check(code: int) -> None:
+    if code != OK:
+        raise GbrError(code, last_error())
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _cuda_tensor(t, name, dtypes):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (this library has no CPU path)" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if t.dtype not in dtypes:
+        raise TypeError("%s has dtype %s, expected one of %s" % (name, t.dtype, dtypes))
+    return t
+
+
+def gemm_bias_relu(A, B, bias, C=None, dtype="bf16", stages=4, stream=None):
+    """C = ReLU(A @ B + bias) on the GPU; returns C."""
+    import torch
+    dt = DTYPE_NAMES[dtype] if isinstance(dtype, str) else int(dtype)
+    in_t = torch.bfloat16 if dt == BF16 else torch.float32
+    _cuda_tensor(A, "A", (in_t,))
+    _cuda_tensor(B, "B", (in_t,))
+    _cuda_tensor(bias, "bias", (torch.float32,))
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(bias.shape) != (N,):
+        raise ValueError("shape mismatch: A %s, B %s, bias %s" % (tuple(A.shape), tuple(B.shape),
+                                                                  tuple(bias.shape)))
+    if C is None:
+        C = torch.empty((M, N), dtype=in_t, device=A.device)
+    _cuda_tensor(C, "C", (in_t,))
+    if tuple(C.shape) != (M, N):
+        raise ValueError("C must be [M, N]")
+    check(lib().gemm_bias_relu(A.data_ptr(), B.data_ptr(), bias.data_ptr(), C.data_ptr(),
+                               M, N, K, dt, int(stages), _stream_ptr(stream)))
+    return C
+
+
+def gemm_bias_relu_grouped(X, W, bias, counts, C=None, stages=4, stream=None):
+    """Per expert e: C[rows of e] = ReLU(X[rows of e] @ W[e] + bias[e]); returns C."""
+    import torch
+    _cuda_tensor(X, "X", (torch.bfloat16,))
+    _cuda_tensor(W, "W", (torch.bfloat16,))
+    _cuda_tensor(bias, "bias", (torch.float32,))
+    G, K, N = W.shape
+    counts = [int(c) for c in counts]
+    if len(counts) != G or X.shape[1] != K or tuple(bias.shape) != (G, N):
+        raise ValueError("shape mismatch")
+    T = sum(counts)
+    if X.shape[0] != T:
+        raise ValueError("X must have sum(counts) rows")
+    if C is None:
+        C = torch.empty((T, N), dtype=torch.bfloat16, device=X.device)
+    _cuda_tensor(C, "C", (torch.bfloat16,))
+    arr = (ctypes.c_int32 * G)(*counts)
+    check(lib().gemm_bias_relu_grouped(X.data_ptr(), W.data_ptr(), bias.data_ptr(), C.data_ptr(),
+                                       ctypes.cast(arr, ctypes.c_void_p), G, K, N, BF16, int(stages),
+                                       _stream_ptr(stream)))
+    return C
+
+
+def staged_copy(src, dst=None, tile=(128, 64), stages=4, stream=None):
+    """dst = src through the TMA staging ring (4-byte elements); returns dst."""
+    import torch
+    ok = (torch.float32, torch.int32)
+    _cuda_tensor(src, "src", ok)
+    if src.dim() != 2:
+        raise ValueError("src must be 2-D")
+    if dst is None:
+        dst = torch.empty_like(src)
+    _cuda_tensor(dst, "dst", ok)
+    if dst.shape != src.shape:
+        raise ValueError("dst must match src")
+    rows, cols = src.shape
+    check(lib().staged_copy(src.data_ptr(), dst.data_ptr(), rows, cols, int(tile[0]), int(tile[1]),
+                            int(stages), _stream_ptr(stream)))
+    return dst
+
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status code."""
+    return int(lib().gbr_device_status(_stream_ptr(stream)))
+
+
+def check_device(stream=None) -> None:
+    check(device_status(stream))
+
+
+def max_stages(op, dtype=0, tile_rows=0, tile_cols=0) -> int:
+    r = int(lib().gbr_max_stages(op, dtype, tile_rows, tile_cols))
+    if r < 0:
+        raise GbrError(-r, last_error())
+    return r
+
+
+def launch_count() -> int:
+    return int(lib().gbr_launch_count())
+
+
+def sm_count() -> int:
+    r = int(lib().gbr_sm_count())
+    if r < 0:
+        raise GbrError(-r, last_error())
+    return r
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    check(lib().gbr_set_wait_timeout_ns(int(ns)))
+
+
+def copy_tuning(store_lag: int = -1, ctas_per_sm: int = -1) -> None:
+    check(lib().gbr_copy_tuning(int(store_lag), int(ctas_per_sm)))
+
+
+def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
+    check(lib().gbr_selftest_wait_timeout(int(timeout_ns), _stream_ptr(stream)))

@@ -1,0 +1,612 @@
+// api.cu -- the C ABI (include/gbr.h): validation, tensor-map encoding,
+// launch configuration and the device status block.
+#include "gbr.h"
+#include "gbr_internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+namespace gbr {
+namespace {
+
+thread_local std::string t_last_error;
+std::atomic<long long> g_launches{0};
+std::mutex g_mu;
+uint64_t g_timeout_ns = 0;  // 0: not yet resolved
+int g_copy_store_lag = -1;
+int g_copy_ctas_per_sm = -1;
+
+constexpr int kMaxDevices = 64;
+
+struct DevCtx {
+    bool ready = false;
+    int sm_count = 0;
+    int smem_optin = 0;
+    uint32_t* status = nullptr;
+    bool ffma_regs_ok = false, ffma_regs_checked = false;
+    bool umma_regs_ok[2][2] = {{false, false}, {false, false}};
+    bool umma_regs_checked[2][2] = {{false, false}, {false, false}};
+};
+DevCtx g_dev[kMaxDevices];
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(GBR_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+uint64_t timeout_ns() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_timeout_ns == 0) {
+        const char* env = std::getenv("GBR_WAIT_TIMEOUT_NS");
+        unsigned long long v = env ? std::strtoull(env, nullptr, 10) : 0ull;
+        g_timeout_ns = v ? v : 2000000000ull;
+    }
+    return g_timeout_ns;
+}
+
+int get_ctx(DevCtx** out, int* dev_out = nullptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(GBR_ERR_INVALID, "device %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevCtx& c = g_dev[dev];
+    if (!c.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&c.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&c.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (major != 10 || minor != 3)
+            return fail(GBR_ERR_UNSUPPORTED,
+                        "device %d is sm_%d%d; this library is built for sm_103a only", dev, major,
+                        minor);
+        if ((e = cudaMalloc(&c.status, kStatusWords * sizeof(uint32_t))) != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(status block)");
+        if ((e = cudaMemset(c.status, 0, kStatusWords * sizeof(uint32_t))) != cudaSuccess)
+            return cuda_fail(e, "cudaMemset(status block)");
+        c.ready = true;
+    }
+    *out = &c;
+    if (dev_out) *dev_out = dev;
+    return GBR_OK;
+}
+
+KernelCtl make_ctl(const DevCtx& c) {
+    KernelCtl k;
+    k.status = c.status;
+    k.timeout_ns = timeout_ns();
+    return k;
+}
+
+// ---------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+int encode(CUtensorMap* map, CUtensorMapDataType dt, uint32_t rank, const void* ptr,
+           const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+           CUtensorMapSwizzle swz, const char* what) {
+    auto fn = encode_fn();
+    if (!fn) return fail(GBR_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    cuuint64_t d[5];
+    cuuint64_t st[4];
+    cuuint32_t b[5], es[5];
+    for (uint32_t i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+    }
+    for (uint32_t i = 0; i + 1 < rank; ++i) st[i] = strides_bytes[i];
+    CUresult r = fn(map, dt, rank, const_cast<void*>(ptr), d, st, b, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(GBR_ERR_INVALID, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what,
+                    int(r));
+    return GBR_OK;
+}
+
+int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
+              uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swz, const char* what) {
+    const uint64_t dims[2] = {inner, outer};
+    const uint64_t strides[1] = {pitch_bytes};
+    const uint32_t box[2] = {box_inner, box_outer};
+    return encode(map, dt, 2, ptr, dims, strides, box, swz, what);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int max_stages_for(size_t (*bytes)(int), int smem_optin) {
+    int s = 0;
+    while (s < 64 && bytes(s + 1) <= size_t(smem_optin)) ++s;
+    return s;
+}
+
+size_t ffma_bytes_fn(int s) { return ffma_smem_bytes(s); }
+size_t umma_bytes_fn(int s) {
+    // The padding that keeps one CTA per SM is not part of the ring budget.
+    return 1024 + size_t(s) * kUmmaStageBytes + kUmmaEpiBytes + 256;
+}
+
+int gemm_max_stages(int dtype, int smem_optin) {
+    return dtype == GBR_F32_FFMA ? max_stages_for(ffma_bytes_fn, smem_optin)
+                                 : max_stages_for(umma_bytes_fn, smem_optin);
+}
+
+int copy_max_stages(uint32_t tile_bytes, int smem_optin) {
+    int s = 0;
+    while (s < 64 && copy_smem_bytes(s + 1, tile_bytes) <= size_t(smem_optin)) ++s;
+    return s;
+}
+
+int check_umma_regs(DevCtx& c, int kind, bool grouped) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!c.umma_regs_checked[kind][grouped]) {
+        int regs = 0;
+        cudaError_t e = umma_check_registers(kind, grouped, &regs);
+        c.umma_regs_checked[kind][grouped] = true;
+        c.umma_regs_ok[kind][grouped] = (e == cudaSuccess);
+        if (e != cudaSuccess && e != cudaErrorInvalidConfiguration)
+            return cuda_fail(e, "cudaFuncGetAttributes(tcgen05 GEMM)");
+    }
+    if (!c.umma_regs_ok[kind][grouped])
+        return fail(GBR_ERR_CUDA,
+                    "tcgen05 GEMM kernel was built with too few registers for its role split");
+    return GBR_OK;
+}
+
+}  // namespace
+}  // namespace gbr
+
+using namespace gbr;
+
+extern "C" {
+
+const char* gbr_last_error(void) { return t_last_error.c_str(); }
+
+long long gbr_launch_count(void) { return g_launches.load(); }
+
+int gbr_sm_count(void) {
+    DevCtx* c;
+    int r = get_ctx(&c);
+    return r == GBR_OK ? c->sm_count : -r;
+}
+
+int gbr_set_wait_timeout_ns(uint64_t ns) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_timeout_ns = 0;
+    if (ns) g_timeout_ns = ns;
+    return GBR_OK;
+}
+
+int gbr_copy_tuning(int store_lag, int ctas_per_sm) {
+    if (store_lag < -1 || store_lag > 1 || ctas_per_sm < -1 || ctas_per_sm == 0)
+        return fail(GBR_ERR_INVALID, "gbr_copy_tuning: store_lag in {-1,0,1}, ctas_per_sm -1 or >= 1");
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_copy_store_lag = store_lag;
+    g_copy_ctas_per_sm = ctas_per_sm;
+    return GBR_OK;
+}
+
+int gbr_max_stages(int op, int dtype, int tile_rows, int tile_cols) {
+    DevCtx* c;
+    int r = get_ctx(&c);
+    if (r != GBR_OK) return -r;
+    if (op == GBR_OP_GEMM) {
+        if (dtype < GBR_F32_FFMA || dtype > GBR_BF16) return -fail(GBR_ERR_INVALID, "bad dtype %d", dtype);
+        return gemm_max_stages(dtype, c->smem_optin);
+    }
+    if (op == GBR_OP_COPY) {
+        if (tile_rows < 1 || tile_rows > 256 || tile_cols < 4 || tile_cols > 256 || tile_cols % 4)
+            return -fail(GBR_ERR_INVALID, "bad copy tile %dx%d", tile_rows, tile_cols);
+        return copy_max_stages(uint32_t(tile_rows) * uint32_t(tile_cols) * 4u, c->smem_optin);
+    }
+    return -fail(GBR_ERR_INVALID, "bad op %d", op);
+}
+
+int gbr_device_status(gbr_stream_t stream) {
+    DevCtx* c;
+    int r = get_ctx(&c);
+    if (r != GBR_OK) return r;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    uint32_t st[kStatusWords];
+    if ((e = cudaMemcpy(st, c->status, sizeof(st), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "reading the status block");
+    if (st[0] == 0) return GBR_OK;
+    if ((e = cudaMemset(c->status, 0, sizeof(st))) != cudaSuccess)
+        return cuda_fail(e, "clearing the status block");
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    return fail(GBR_ERR_TIMEOUT,
+                "a pipeline wait timed out (site 0x%02x, CTA %u, item %u); that call's output "
+                "is undefined",
+                st[1], st[2], st[3]);
+}
+
+int gbr_selftest_wait_timeout(uint64_t timeout_ns_limit, gbr_stream_t stream) {
+    DevCtx* c;
+    int r = get_ctx(&c);
+    if (r != GBR_OK) return r;
+    if (timeout_ns_limit == 0 || timeout_ns_limit > 10000000000ull)
+        return fail(GBR_ERR_INVALID, "self-test limit must be in (0, 10 s]");
+    KernelCtl ctl = make_ctl(*c);
+    ctl.timeout_ns = timeout_ns_limit;
+    cudaError_t e = launch_wait_selftest(ctl, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "launching the wait self-test");
+    ++g_launches;
+    return GBR_OK;
+}
+
+int staged_copy(const void* src, void* dst, int64_t rows, int64_t cols, int tile_rows,
+                int tile_cols, int stages, gbr_stream_t stream) {
+    if (rows < 0 || cols < 0 || rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31))
+        return fail(GBR_ERR_INVALID, "staged_copy: rows/cols must be in [0, 2^31)");
+    if (tile_rows < 1 || tile_rows > 256 || tile_cols < 4 || tile_cols > 256)
+        return fail(GBR_ERR_INVALID, "staged_copy: tile must be 1..256 x 4..256");
+    if (tile_cols % 4) return fail(GBR_ERR_ALIGN, "staged_copy: tile_cols must be a multiple of 4");
+    DevCtx* c;
+    int r = get_ctx(&c);
+    if (r != GBR_OK) return r;
+    const uint32_t tile_bytes = uint32_t(tile_rows) * uint32_t(tile_cols) * 4u;
+    const int smax = copy_max_stages(tile_bytes, c->smem_optin);
+    if (stages < 1 || stages > smax)
+        return fail(GBR_ERR_SMEM, "staged_copy: stages=%d outside [1, %d] for a %dx%d fp32 tile",
+                    stages, smax, tile_rows, tile_cols);
+    if (rows == 0 || cols == 0) return GBR_OK;
+    if (!src || !dst) return fail(GBR_ERR_INVALID, "staged_copy: NULL buffer");
+    if (!aligned16(src) || !aligned16(dst))
+        return fail(GBR_ERR_ALIGN, "staged_copy: buffers must be 16-byte aligned");
+    if (cols % 4) return fail(GBR_ERR_ALIGN, "staged_copy: cols must be a multiple of 4");
+    const size_t bytes = size_t(rows) * size_t(cols) * 4u;
+    if (overlaps(src, bytes, dst, bytes)) return fail(GBR_ERR_INVALID, "staged_copy: src and dst overlap");
+
+    CUtensorMap ms, md;
+    if ((r = encode_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, src, uint64_t(cols), uint64_t(rows),
+                       uint64_t(cols) * 4u, uint32_t(tile_cols), uint32_t(tile_rows),
+                       CU_TENSOR_MAP_SWIZZLE_NONE, "copy src")) != GBR_OK)
+        return r;
+    if ((r = encode_2d(&md, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dst, uint64_t(cols), uint64_t(rows),
+                       uint64_t(cols) * 4u, uint32_t(tile_cols), uint32_t(tile_rows),
+                       CU_TENSOR_MAP_SWIZZLE_NONE, "copy dst")) != GBR_OK)
+        return r;
+
+    CopyArgs a;
+    a.rows = int32_t(rows);
+    a.cols = int32_t(cols);
+    a.tile_rows = tile_rows;
+    a.tile_cols = tile_cols;
+    a.tiles_c = int32_t(cdiv(cols, tile_cols));
+    a.num_tiles = cdiv(rows, tile_rows) * int64_t(a.tiles_c);
+    a.stages = stages;
+    a.tile_bytes = tile_bytes;
+    int lag, cps;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        lag = g_copy_store_lag;
+        cps = g_copy_ctas_per_sm;
+    }
+    a.store_lag = (lag < 0) ? (stages >= 2 ? 1 : 0) : lag;
+    if (a.store_lag == 1 && stages < 2) a.store_lag = 0;
+    a.ctl = make_ctl(*c);
+
+    const size_t smem = copy_smem_bytes(stages, tile_bytes);
+    cudaError_t e = copy_prepare(smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(staged copy)");
+    int occ = 0;
+    if ((e = copy_occupancy(smem, &occ)) != cudaSuccess) return cuda_fail(e, "occupancy(staged copy)");
+    if (occ < 1) return fail(GBR_ERR_SMEM, "staged_copy: kernel does not fit on an SM");
+    if (cps > 0 && cps < occ) occ = cps;
+    const int64_t grid = std::min<int64_t>(a.num_tiles, int64_t(c->sm_count) * occ);
+    e = launch_staged_copy(ms, md, a, int(grid), smem, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "launching staged copy");
+    ++g_launches;
+    return GBR_OK;
+}
+
+int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int64_t M, int64_t N,
+                   int64_t K, int dtype, int stages, gbr_stream_t stream) {
+    if (dtype < GBR_F32_FFMA || dtype > GBR_BF16)
+        return fail(GBR_ERR_INVALID, "gemm_bias_relu: unknown dtype %d", dtype);
+    const int64_t lim = int64_t(1) << 31;
+    if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim)
+        return fail(GBR_ERR_INVALID, "gemm_bias_relu: M, N, K must be in [0, 2^31)");
+    DevCtx* c;
+    int r = get_ctx(&c);
+    if (r != GBR_OK) return r;
+    const int smax = gemm_max_stages(dtype, c->smem_optin);
+    if (stages < 1 || stages > smax)
+        return fail(GBR_ERR_SMEM, "gemm_bias_relu: stages=%d outside [1, %d] for dtype %d", stages,
+                    smax, dtype);
+    if (M == 0 || N == 0) return GBR_OK;
+    const uint64_t es = dtype == GBR_BF16 ? 2 : 4;
+    if (!C || !bias || (K > 0 && (!A || !B)))
+        return fail(GBR_ERR_INVALID, "gemm_bias_relu: NULL buffer");
+    if (!aligned16(C) || !aligned16(bias) || (K > 0 && (!aligned16(A) || !aligned16(B))))
+        return fail(GBR_ERR_ALIGN, "gemm_bias_relu: buffers must be 16-byte aligned");
+    if ((uint64_t(N) * es) % 16 || (uint64_t(K) * es) % 16)
+        return fail(GBR_ERR_ALIGN,
+                    "gemm_bias_relu: row pitches K*%d and N*%d bytes must be multiples of 16",
+                    int(es), int(es));
+    const size_t c_bytes = size_t(M) * size_t(N) * es;
+    if ((K > 0 && (overlaps(C, c_bytes, A, size_t(M) * K * es) ||
+                   overlaps(C, c_bytes, B, size_t(K) * N * es))) ||
+        overlaps(C, c_bytes, bias, size_t(N) * 4))
+        return fail(GBR_ERR_INVALID, "gemm_bias_relu: C overlaps an input");
+
+    GemmShape s;
+    memset(&s, 0, sizeof(s));
+    s.M = int32_t(M);
+    s.N = int32_t(N);
+    s.K = int32_t(K);
+    s.stages = stages;
+    s.bias = bias;
+    s.C = C;
+    s.ctl = make_ctl(*c);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+
+    if (dtype == GBR_F32_FFMA) {
+        s.m_tiles = int32_t(cdiv(M, kFfmaBM));
+        s.n_tiles = int32_t(cdiv(N, kFfmaBN));
+        s.num_kb = int32_t(cdiv(K, kFfmaBK));
+        s.num_tiles = s.m_tiles * s.n_tiles;
+        s.group_m = 8;
+        CUtensorMap ma, mb;
+        const void* pa = K > 0 ? A : C;
+        const void* pb = K > 0 ? B : C;
+        const uint64_t kk = K > 0 ? uint64_t(K) : uint64_t(N);
+        if ((r = encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, pa, kk, uint64_t(M), kk * 4, 32,
+                           128, CU_TENSOR_MAP_SWIZZLE_128B, "A")) != GBR_OK)
+            return r;
+        if ((r = encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, pb, uint64_t(N),
+                           K > 0 ? uint64_t(K) : uint64_t(M), uint64_t(N) * 4, 32, 32,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "B")) != GBR_OK)
+            return r;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            if (!c->ffma_regs_checked) {
+                int regs = 0;
+                e = ffma_check_registers(&regs);
+                c->ffma_regs_checked = true;
+                c->ffma_regs_ok = (e == cudaSuccess);
+                if (e != cudaSuccess && e != cudaErrorInvalidConfiguration)
+                    return cuda_fail(e, "cudaFuncGetAttributes(FFMA GEMM)");
+            }
+            if (!c->ffma_regs_ok)
+                return fail(GBR_ERR_CUDA, "FFMA GEMM kernel was built with too few registers for its role split");
+        }
+        const size_t smem = ffma_smem_bytes(stages);
+        if ((e = ffma_prepare(smem)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(FFMA)");
+        int occ = 0;
+        if ((e = ffma_occupancy(smem, &occ)) != cudaSuccess) return cuda_fail(e, "occupancy(FFMA)");
+        if (occ < 1) return fail(GBR_ERR_SMEM, "FFMA GEMM does not fit on an SM");
+        const int grid = int(std::min<int64_t>(s.num_tiles, int64_t(c->sm_count) * occ));
+        if ((e = launch_gemm_ffma(ma, mb, s, grid, smem, st)) != cudaSuccess)
+            return cuda_fail(e, "launching FFMA GEMM");
+        ++g_launches;
+        return GBR_OK;
+    }
+
+    const int kind = dtype == GBR_BF16 ? kUmmaBf16 : kUmmaTf32;
+    const CUtensorMapDataType dt =
+        dtype == GBR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const uint32_t bk = uint32_t(128 / es);          // K per stage
+    const uint32_t panel_cols = uint32_t(128 / es);  // B panel width; also the C store box width
+    s.m_tiles = int32_t(cdiv(M, kUmmaBM));
+    s.n_tiles = int32_t(cdiv(N, kUmmaBN));
+    s.num_kb = int32_t(cdiv(K, bk));
+    s.num_tiles = s.m_tiles * s.n_tiles;
+    s.group_m = 16;
+    CUtensorMap ma, mb, mc;
+    if ((r = encode_2d(&mc, dt, C, uint64_t(N), uint64_t(M), uint64_t(N) * es, panel_cols, 32,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "C")) != GBR_OK)
+        return r;
+    if ((r = check_umma_regs(*c, kind, false)) != GBR_OK) return r;
+    const size_t smem = umma_smem_bytes(stages);
+    if ((e = umma_prepare(kind, false, smem)) != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute(tcgen05 GEMM)");
+    const int grid = int(std::min<int64_t>(s.num_tiles, c->sm_count));
+    float* bt = nullptr;  // TF32 only: K-major copy of B, stream-ordered scratch
+    if (K > 0) {
+        if ((r = encode_2d(&ma, dt, A, uint64_t(K), uint64_t(M), uint64_t(K) * es, bk, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "A")) != GBR_OK)
+            return r;
+        if (kind == kUmmaBf16) {
+            if ((r = encode_2d(&mb, dt, B, uint64_t(N), uint64_t(K), uint64_t(N) * es, panel_cols,
+                               bk, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != GBR_OK)
+                return r;
+        } else {
+            if ((e = cudaMallocAsync(reinterpret_cast<void**>(&bt), size_t(K) * size_t(N) * 4, st)) !=
+                cudaSuccess)
+                return cuda_fail(e, "cudaMallocAsync(TF32 B transpose)");
+            if ((r = encode_2d(&mb, dt, bt, uint64_t(K), uint64_t(N), uint64_t(K) * es, bk, 256,
+                               CU_TENSOR_MAP_SWIZZLE_128B, "Bt")) != GBR_OK) {
+                cudaFreeAsync(bt, st);
+                return r;
+            }
+            if ((e = launch_transpose_f32(static_cast<const float*>(B), bt, int(K), int(N), st)) !=
+                cudaSuccess) {
+                cudaFreeAsync(bt, st);
+                return cuda_fail(e, "launching the B transpose");
+            }
+            ++g_launches;
+        }
+    } else {
+        ma = mc;  // never read: no k-blocks are loaded when K == 0
+        mb = mc;
+    }
+    e = launch_gemm_umma(kind, ma, mb, mc, s, grid, smem, st);
+    if (bt) cudaFreeAsync(bt, st);
+    if (e != cudaSuccess) return cuda_fail(e, "launching tcgen05 GEMM");
+    ++g_launches;
+    return GBR_OK;
+}
+
+int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void* C,
+                           const int32_t* counts_host, int num_groups, int64_t K, int64_t N,
+                           int dtype, int stages, gbr_stream_t stream) {
+    if (dtype != GBR_BF16)
+        return fail(GBR_ERR_UNSUPPORTED, "gemm_bias_relu_grouped: only GBR_BF16 is built");
+    if (num_groups < 1 || num_groups > kMaxGroups)
+        return fail(GBR_ERR_INVALID, "gemm_bias_relu_grouped: num_groups must be 1..%d", kMaxGroups);
+    if (!counts_host) return fail(GBR_ERR_INVALID, "gemm_bias_relu_grouped: NULL counts");
+    const int64_t lim = int64_t(1) << 31;
+    if (K < 0 || N < 0 || K >= lim || N >= lim)
+        return fail(GBR_ERR_INVALID, "gemm_bias_relu_grouped: K, N must be in [0, 2^31)");
+    int64_t T = 0;
+    for (int e = 0; e < num_groups; ++e) {
+        if (counts_host[e] < 0) return fail(GBR_ERR_INVALID, "gemm_bias_relu_grouped: negative count");
+        T += counts_host[e];
+    }
+    if (T >= lim) return fail(GBR_ERR_INVALID, "gemm_bias_relu_grouped: too many rows");
+    DevCtx* c;
+    int r = get_ctx(&c);
+    if (r != GBR_OK) return r;
+    const int smax = gemm_max_stages(dtype, c->smem_optin);
+    if (stages < 1 || stages > smax)
+        return fail(GBR_ERR_SMEM, "gemm_bias_relu_grouped: stages=%d outside [1, %d]", stages, smax);
+    if (T == 0 || N == 0) return GBR_OK;
+    const uint64_t es = 2;
+    if (!C || !bias || (K > 0 && (!X || !W)))
+        return fail(GBR_ERR_INVALID, "gemm_bias_relu_grouped: NULL buffer");
+    if (!aligned16(C) || !aligned16(bias) || (K > 0 && (!aligned16(X) || !aligned16(W))))
+        return fail(GBR_ERR_ALIGN, "gemm_bias_relu_grouped: buffers must be 16-byte aligned");
+    if ((uint64_t(N) * es) % 16 || (uint64_t(K) * es) % 16)
+        return fail(GBR_ERR_ALIGN, "gemm_bias_relu_grouped: K and N must be multiples of 8");
+    const size_t c_bytes = size_t(T) * size_t(N) * es;
+    if ((K > 0 && (overlaps(C, c_bytes, X, size_t(T) * K * es) ||
+                   overlaps(C, c_bytes, W, size_t(num_groups) * K * N * es))) ||
+        overlaps(C, c_bytes, bias, size_t(num_groups) * N * 4))
+        return fail(GBR_ERR_INVALID, "gemm_bias_relu_grouped: C overlaps an input");
+
+    GemmShape s;
+    memset(&s, 0, sizeof(s));
+    s.M = int32_t(T);
+    s.N = int32_t(N);
+    s.K = int32_t(K);
+    s.stages = stages;
+    s.bias = bias;
+    s.C = C;
+    s.ctl = make_ctl(*c);
+    s.n_tiles = int32_t(cdiv(N, kUmmaBN));
+    s.num_kb = int32_t(cdiv(K, 64));
+    s.group_m = 16;
+    GroupTable g;
+    memset(&g, 0, sizeof(g));
+    g.num_groups = num_groups;
+    CUtensorMap mc[kMaxGroups];
+    int64_t off = 0, tiles = 0;
+    int last_valid = -1;
+    for (int e = 0; e < num_groups; ++e) {
+        const int64_t n_e = counts_host[e];
+        g.row_off[e] = int32_t(off);
+        g.rows[e] = int32_t(n_e);
+        g.m_tiles[e] = int32_t(cdiv(n_e, kUmmaBM));
+        g.tile_start[e] = int32_t(tiles);
+        tiles += int64_t(g.m_tiles[e]) * s.n_tiles;
+        if (n_e > 0) {
+            const void* base = static_cast<const uint8_t*>(C) + size_t(off) * size_t(N) * es;
+            if ((r = encode_2d(&mc[e], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, uint64_t(N),
+                               uint64_t(n_e), uint64_t(N) * es, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B,
+                               "C[e]")) != GBR_OK)
+                return r;
+            last_valid = e;
+        }
+        off += n_e;
+    }
+    for (int e = 0; e < num_groups; ++e)
+        if (counts_host[e] == 0) mc[e] = mc[last_valid];  // never used: the group has no tiles
+    g.tile_start[num_groups] = int32_t(tiles);
+    s.num_tiles = int32_t(tiles);
+    s.m_tiles = 0;
+    CUtensorMap mx, mw;
+    if (K > 0) {
+        if ((r = encode_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, uint64_t(K), uint64_t(T),
+                           uint64_t(K) * es, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "X")) != GBR_OK)
+            return r;
+        const uint64_t dims[3] = {uint64_t(N), uint64_t(K), uint64_t(num_groups)};
+        const uint64_t strides[2] = {uint64_t(N) * es, uint64_t(K) * uint64_t(N) * es};
+        const uint32_t box[3] = {64, 64, 1};
+        if ((r = encode(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, W, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "W")) != GBR_OK)
+            return r;
+    } else {
+        mx = mc[last_valid];
+        mw = mc[last_valid];
+    }
+    if ((r = check_umma_regs(*c, kUmmaBf16, true)) != GBR_OK) return r;
+    const size_t smem = umma_smem_bytes(stages);
+    cudaError_t e = umma_prepare(kUmmaBf16, true, smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(grouped GEMM)");
+    const int grid = int(std::min<int64_t>(s.num_tiles, c->sm_count));
+    if ((e = launch_gemm_umma_grouped(mx, mw, mc, g, s, int64_t(N), grid, smem,
+                                      reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
+        return cuda_fail(e, "launching grouped GEMM");
+    ++g_launches;
+    return GBR_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- self test
+namespace gbr {
+namespace {
+__global__ void wait_selftest_kernel(KernelCtl ctl) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_addr(&bar), 1);
+        abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // Nothing ever arrives on `bar`: the bounded wait must give up.
+        mbar_wait(ptx::smem_addr(&bar), 0, ctl, &abort_flag, kSiteSelfTest, 0);
+    }
+    __syncthreads();
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(KernelCtl ctl, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(ctl);
+    return cudaGetLastError();
+}
+}  // namespace gbr

@@ -1,0 +1,107 @@
+// gbr_common.cuh -- pieces shared by every pipeline kernel: the bounded
+// mbarrier wait, the device status block and the persistent tile order.
+#pragma once
+#include <cstdint>
+#include "gbr_ptx.cuh"
+
+namespace gbr {
+
+// Device status block, one per device (kStatusWords 32-bit words):
+//   [0] error bits (kDevErrTimeout), [1] code of the first wait that gave up,
+//   [2] its CTA index, [3] its item/iteration index.
+constexpr int kStatusWords = 16;
+constexpr uint32_t kDevErrTimeout = 1u;
+
+// Wait-site codes recorded in status[1] (role << 4 | which barrier).
+enum WaitSite : uint32_t {
+    kSiteProducerEmpty = 0x11,
+    kSiteProducerDrain = 0x12,
+    kSiteConsumerFull = 0x21,
+    kSiteMmaFull = 0x31,
+    kSiteMmaAccEmpty = 0x32,
+    kSiteMmaDrain = 0x33,
+    kSiteEpiAccFull = 0x41,
+    kSiteStorerFull = 0x51,
+    kSiteSelfTest = 0x71,
+};
+
+struct KernelCtl {
+    uint32_t* status;          // device status block (kStatusWords words)
+    uint64_t timeout_ns;       // per-wait limit on %globaltimer
+};
+
+// Iteration cap of one bounded wait; the time limit normally ends it first.
+constexpr uint32_t kMaxPollIters = 1u << 26;
+
+__device__ __forceinline__ void record_timeout(const KernelCtl& ctl, uint32_t site, uint32_t item) {
+    atomicOr(ctl.status + 0, kDevErrTimeout);
+    if (atomicCAS(ctl.status + 1, 0u, site) == 0u) {
+        ctl.status[2] = blockIdx.x;
+        ctl.status[3] = item;
+    }
+}
+
+// Slow path of a bounded wait: polls until the phase completes, another role
+// raised the CTA's abort flag, or the time/iteration limit runs out (then it
+// records the site, raises the abort flag and gives up).
+__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
+                                            volatile int* abort_flag, uint32_t site,
+                                            uint32_t item) {
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t iter = 0; iter < kMaxPollIters; ++iter) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > ctl.timeout_ns) break;
+    }
+    *abort_flag = 1;
+    record_timeout(ctl, site, item);
+    return false;
+}
+
+// Bounded wait for the phase of `bar` with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
+                                          volatile int* abort_flag, uint32_t site, uint32_t item) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, ctl, abort_flag, site, item);
+}
+
+// The same wait taken by all 32 lanes of a warp.  The outcome is made
+// warp-uniform, so a warp never splits into lanes that carry on and lanes that
+// abort (the warp-wide .sync.aligned instructions that follow need every lane).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
+                                               volatile int* abort_flag, uint32_t site,
+                                               uint32_t item) {
+    const bool ok = mbar_wait(bar, parity, ctl, abort_flag, site, item);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Wait used only while tearing down after an abort: bounded, records nothing
+// new and ignores the abort flag (it waits for this CTA's own copies in flight).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t iter = 0; iter < kMaxPollIters; ++iter) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (ptx::globaltimer() - t0 > limit_ns) return false;
+    }
+    return false;
+}
+
+// Persistent tile order over an (m_tiles x n_tiles) grid of output tiles:
+// bands of `group_m` tile rows, column-major inside a band, so that the CTAs
+// running at the same time share A rows and B columns in L2.
+__device__ __forceinline__ void raster_tile(uint32_t t, uint32_t m_tiles, uint32_t n_tiles,
+                                            uint32_t group_m, uint32_t& mt, uint32_t& nt) {
+    const uint32_t band = group_m * n_tiles;
+    const uint32_t g = t / band;
+    const uint32_t first_m = g * group_m;
+    const uint32_t rows = min(group_m, m_tiles - first_m);
+    const uint32_t r = t - g * band;
+    mt = first_m + r % rows;
+    nt = r / rows;
+}
+
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+}  // namespace gbr

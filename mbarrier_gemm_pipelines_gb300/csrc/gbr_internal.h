@@ -1,0 +1,89 @@
+// gbr_internal.h -- host-side interface between the C ABI (api.cu) and the
+// kernel translation units.  Not installed; not part of the public ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gbr_common.cuh"
+
+namespace gbr {
+
+// ------------------------------------------------------------ staged copy
+struct CopyArgs {
+    int32_t rows, cols;            // fp32 elements
+    int32_t tile_rows, tile_cols;  // TMA box
+    int32_t tiles_c;               // tiles per row of tiles
+    int64_t num_tiles;
+    int32_t stages;
+    uint32_t tile_bytes;
+    int32_t store_lag;             // 0: release a slot when its own store has read it
+                                   // 1: release the previous slot after issuing the next store
+    KernelCtl ctl;
+};
+
+size_t copy_smem_bytes(int stages, uint32_t tile_bytes);
+cudaError_t copy_prepare(size_t smem);                 // per-device function attributes
+cudaError_t copy_occupancy(size_t smem, int* blocks_per_sm);
+cudaError_t launch_staged_copy(const CUtensorMap& src, const CUtensorMap& dst, const CopyArgs& a,
+                               int grid, size_t smem, cudaStream_t stream);
+
+// ------------------------------------------------------------ GEMM common
+struct GemmShape {
+    int32_t M, N, K;
+    int32_t m_tiles, n_tiles, num_kb;
+    int32_t num_tiles;
+    int32_t stages;
+    int32_t group_m;
+    const float* bias;
+    void* C;                       // used by epilogues that store with st.global
+    KernelCtl ctl;
+};
+
+// FFMA path (strict fp32, CUDA cores): 128x128x32 tiles.
+constexpr int kFfmaBM = 128, kFfmaBN = 128, kFfmaBK = 32;
+constexpr uint32_t kFfmaStageBytes = (kFfmaBM + kFfmaBN) * kFfmaBK * 4;
+size_t ffma_smem_bytes(int stages);
+cudaError_t ffma_prepare(size_t smem);
+cudaError_t ffma_occupancy(size_t smem, int* blocks_per_sm);
+cudaError_t ffma_check_registers(int* regs);
+cudaError_t launch_gemm_ffma(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmShape& s,
+                             int grid, size_t smem, cudaStream_t stream);
+
+// tcgen05 path: 128x256 output tiles, 128-byte K slices per stage.
+constexpr int kUmmaBM = 128, kUmmaBN = 256;
+constexpr uint32_t kUmmaAStageBytes = kUmmaBM * 128;        // 16 KiB
+constexpr uint32_t kUmmaBStageBytes = kUmmaBN * 128;        // 32 KiB
+constexpr uint32_t kUmmaStageBytes = kUmmaAStageBytes + kUmmaBStageBytes;
+constexpr uint32_t kUmmaEpiBytes = 4 * 2 * 32 * 128;        // 4 warps x 2 buffers x 4 KiB
+constexpr int kMaxGroups = 32;
+
+enum UmmaKind : int { kUmmaBf16 = 0, kUmmaTf32 = 1 };
+
+struct GroupTable {
+    int32_t num_groups;
+    int32_t row_off[kMaxGroups];       // first row of group e in X and C
+    int32_t rows[kMaxGroups];          // n_e
+    int32_t m_tiles[kMaxGroups];       // ceil(n_e / 128)
+    int32_t tile_start[kMaxGroups + 1];  // prefix sum of m_tiles[e] * n_tiles
+};
+
+size_t umma_smem_bytes(int stages);
+cudaError_t umma_prepare(int kind, bool grouped, size_t smem);
+cudaError_t umma_check_registers(int kind, bool grouped, int* regs);
+cudaError_t launch_gemm_umma(int kind, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                             const CUtensorMap& mapC, const GemmShape& s, int grid, size_t smem,
+                             cudaStream_t stream);
+cudaError_t launch_gemm_umma_grouped(const CUtensorMap& mapX, const CUtensorMap& mapW,
+                                     const CUtensorMap* mapsC, const GroupTable& g,
+                                     const GemmShape& s, int64_t bias_group_stride, int grid,
+                                     size_t smem, cudaStream_t stream);
+
+// Bt[N, K] = B[K, N], 32-bit elements, K and N multiples of 4.
+cudaError_t launch_transpose_f32(const float* B, float* Bt, int K, int N, cudaStream_t stream);
+
+// ------------------------------------------------------------ self test
+cudaError_t launch_wait_selftest(KernelCtl ctl, cudaStream_t stream);
+
+}  // namespace gbr

@@ -1,0 +1,217 @@
+// gemm_ffma.cu -- warp-specialized fp32 GEMM + bias + ReLU on CUDA cores.
+//
+// The SGEMM test bench of "pwwt.cn news/4436243", section 4.1: A[M,K] and
+// B[K,N] fp32, C[M,N] = ReLU(A*B + bias), with the K loop turned into the
+// ring buffer of section 3.4: a producer role moves K tiles into a stage ring
+// while consumer roles compute on full stages and hand them back.
+//
+// Roles (one CTA = 3 warpgroups, 384 threads, "gpu_warp_specialization",
+// "The architecture: every piece explained": whole warps take whole jobs,
+// and the register budget moves from the producers to the consumers):
+//   warpgroup 0  warp 0 lane 0 = TMA producer; the group gives up registers
+//   warpgroups 1-2 (8 warps)   = FFMA consumers, one 8x8 register micro-tile
+//                                 per thread of a 128x128 output tile
+// Ring: S stages of { A 128x32 fp32, 128-byte swizzled rows;
+//                     B 32x128 fp32 as four 32-column 128-byte swizzled panels }.
+// full[s]: 1 arrival (producer's arrive.expect_tx) + 32 KiB of TMA bytes.
+// empty[s]: 8 arrivals, one per consumer warp after its last read of the slot.
+// Slot/parity of k-iteration i (running across this CTA's tiles):
+//   slot = i % S, full parity = (i / S) & 1, empty parity = ((i / S) & 1) ^ 1.
+#include "gbr_internal.h"
+
+namespace gbr {
+
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kConsumerWarps = 8;
+constexpr uint32_t kABytes = kFfmaBM * kFfmaBK * 4;   // 16 KiB
+constexpr uint32_t kBPanelBytes = kFfmaBK * 128;      // 32 rows x 128 B
+constexpr uint32_t kProducerRegs = 40;
+constexpr uint32_t kConsumerRegs = 232;
+
+// Byte offset of A(m, k) inside a stage: 128-byte rows (32 fp32 of K), the
+// 16-byte chunk index XOR-ed with (m % 8) by the TMA 128-byte swizzle.
+__device__ __forceinline__ uint32_t a_off(uint32_t m, uint32_t k4) {
+    return m * 128u + ((k4 ^ (m & 7u)) << 4);
+}
+// Byte offset of B(k, n..n+3) (n % 4 == 0): 32-column panels of 32 rows.
+__device__ __forceinline__ uint32_t b_off(uint32_t k, uint32_t n) {
+    return (n >> 5) * kBPanelBytes + k * 128u + ((((n & 31u) >> 2) ^ (k & 7u)) << 4);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_ffma_kernel(const __grid_constant__ CUtensorMap mapA,
+                     const __grid_constant__ CUtensorMap mapB, const GemmShape p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = align_1024(smem_raw);
+    const int S = p.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + size_t(S) * kFfmaStageBytes);
+    uint64_t* empty = full + S;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
+
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(ptx::smem_addr(full + s), 1);
+            ptx::mbar_init(ptx::smem_addr(empty + s), kConsumerWarps);
+        }
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    } else if (threadIdx.x == 32) {
+        ptx::prefetch_tensormap(&mapA);
+        ptx::prefetch_tensormap(&mapB);
+    }
+    __syncthreads();
+
+    const uint32_t ring_base = ptx::smem_addr(ring);
+
+    if (warp < 4) {
+        ptx::setmaxnreg_dec<kProducerRegs>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------ producer
+            uint32_t i = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                uint32_t mt, nt;
+                raster_tile(t, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+                for (int kb = 0; kb < p.num_kb; ++kb, ++i) {
+                    const uint32_t s = i % S, ph = (i / S) & 1u;
+                    if (!mbar_wait(ptx::smem_addr(empty + s), ph ^ 1u, p.ctl, abort_flag,
+                                   kSiteProducerEmpty, i)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = ptx::smem_addr(full + s);
+                    ptx::mbar_arrive_expect_tx(fb, kFfmaStageBytes);
+                    const uint32_t st = ring_base + s * kFfmaStageBytes;
+                    ptx::tma_load_2d(st, &mapA, fb, kb * kFfmaBK, int(mt) * kFfmaBM);
+#pragma unroll
+                    for (int j = 0; j < kFfmaBN / 32; ++j)
+                        ptx::tma_load_2d(st + kABytes + j * kBPanelBytes, &mapB, fb,
+                                         int(nt) * kFfmaBN + 32 * j, kb * kFfmaBK);
+                }
+            }
+            if (*abort_flag) {
+                const uint32_t n = i < uint32_t(S) ? i : uint32_t(S);
+                for (uint32_t j = i - n; j < i; ++j)
+                    mbar_wait_drain(ptx::smem_addr(full + j % S), (j / S) & 1u, p.ctl.timeout_ns);
+            }
+        }
+    } else {
+        ptx::setmaxnreg_inc<kConsumerRegs>();
+        // ---------------------------------------------------- consumers
+        const uint32_t ct = threadIdx.x - 128;        // 0..255
+        const uint32_t tx = ct & 15u, ty = ct >> 4;   // 16 x 16 threads
+        // Rows 4ty..4ty+3 and 64+4ty..; columns 4tx..4tx+3 and 64+4tx..
+        uint32_t a_row[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) a_row[r] = (r < 4 ? 0u : 64u) + 4u * ty + (r & 3);
+        const uint32_t n_lo = 4u * tx, n_hi = 64u + 4u * tx;
+
+        uint32_t i = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            uint32_t mt, nt;
+            raster_tile(t, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+            float acc[8][8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+
+            for (int kb = 0; kb < p.num_kb; ++kb, ++i) {
+                const uint32_t s = i % S, ph = (i / S) & 1u;
+                if (!mbar_wait_warp(ptx::smem_addr(full + s), ph, p.ctl, abort_flag,
+                                    kSiteConsumerFull, i)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* As = ring + size_t(s) * kFfmaStageBytes;
+                const uint8_t* Bs = As + kABytes;
+#pragma unroll 2
+                for (uint32_t k4 = 0; k4 < kFfmaBK / 4; ++k4) {
+                    float4 a[8];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r)
+                        a[r] = *reinterpret_cast<const float4*>(As + a_off(a_row[r], k4));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t k = 4 * k4 + kk;
+                        const float4 b0 = *reinterpret_cast<const float4*>(Bs + b_off(k, n_lo));
+                        const float4 b1 = *reinterpret_cast<const float4*>(Bs + b_off(k, n_hi));
+                        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) {
+                            const float av = kk == 0 ? a[r].x : kk == 1 ? a[r].y
+                                           : kk == 2 ? a[r].z : a[r].w;
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av, bv[c], acc[r][c]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(empty + s));
+            }
+            if (!ok) break;
+
+            // ------------------------------------------------ epilogue
+            float* C = static_cast<float*>(p.C);
+            const int n0 = int(nt) * kFfmaBN, m0 = int(mt) * kFfmaBM;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int n = n0 + int(h == 0 ? n_lo : n_hi);
+                if (n >= p.N) continue;
+                const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + n));
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int m = m0 + int(a_row[r]);
+                    if (m >= p.M) continue;
+                    float4 v;
+                    v.x = fmaxf(acc[r][4 * h + 0] + bb.x, 0.f);
+                    v.y = fmaxf(acc[r][4 * h + 1] + bb.y, 0.f);
+                    v.z = fmaxf(acc[r][4 * h + 2] + bb.z, 0.f);
+                    v.w = fmaxf(acc[r][4 * h + 3] + bb.w, 0.f);
+                    *reinterpret_cast<float4*>(C + size_t(m) * p.N + n) = v;
+                }
+            }
+        }
+    }
+    __syncwarp();
+    __syncthreads();
+}
+
+}  // namespace
+
+size_t ffma_smem_bytes(int stages) {
+    return 1024 + size_t(stages) * kFfmaStageBytes + size_t(2 * stages) * 8 + 16;
+}
+
+cudaError_t ffma_prepare(size_t smem) {
+    return cudaFuncSetAttribute(gemm_ffma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(smem));
+}
+
+cudaError_t ffma_occupancy(size_t smem, int* blocks_per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, gemm_ffma_kernel,
+                                                         kThreads, smem);
+}
+
+// The register split must fit in what the CTA is launched with, or the
+// consumers' setmaxnreg.inc would wait forever for registers.
+cudaError_t ffma_check_registers(int* regs) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, gemm_ffma_kernel);
+    if (e != cudaSuccess) return e;
+    *regs = fa.numRegs;
+    const long need = 128L * kProducerRegs + 256L * kConsumerRegs;
+    return (long(fa.numRegs) * kThreads >= need) ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
+cudaError_t launch_gemm_ffma(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmShape& s,
+                             int grid, size_t smem, cudaStream_t stream) {
+    gemm_ffma_kernel<<<grid, kThreads, smem, stream>>>(mapA, mapB, s);
+    return cudaGetLastError();
+}
+
+}  // namespace gbr

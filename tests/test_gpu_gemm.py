@@ -1,0 +1,186 @@
+"""GEMM + bias + ReLU on the GPU (through the C ABI) against the binary64 oracle.
+
+Bars (relative Frobenius error): FFMA 1e-5, TF32 5e-3, bf16 1e-2.  Small
+problems are compared element by element in full; the full-size workloads
+(fp32 4096^3, bf16 8192^3) at sampled positions the oracle evaluates one by one,
+in the same launch configuration the benchmark uses."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mbarrier_gemm_pipelines_gb300 import inputs
+from gpu_helpers import (TOL, load_library, rel_frobenius, require_gpu, sample_points,
+                         to_host_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gbr():
+    require_gpu()
+    return load_library()
+
+
+def _run(gbr, A, B, bias, dtype, stages):
+    C = gbr.gemm_bias_relu(A.cuda(), B.cuda(), bias.cuda(), dtype=dtype, stages=stages)
+    gbr.check_device()
+    return to_host_f64(C)
+
+
+def _check_full(got, A, B, bias, dtype):
+    ref = oracle.gemm_bias_relu(A, B, bias)
+    err = rel_frobenius(got, ref)
+    assert err <= TOL[dtype], err
+    assert (got >= 0).all()
+    # element-wise: no single output far off (catches a wrong tile at a ragged edge)
+    scale = np.abs(ref).max() + 1e-30
+    assert np.abs(got - ref).max() <= 20 * TOL[dtype] * scale
+    return err
+
+
+def test_config1_ffma_256_s2(gbr):
+    """fp32 256^3, U[-1,1] from seed 0, 2-stage ring, BK = 32."""
+    A, B, bias = inputs.workload("gemm_small")
+    got = _run(gbr, A, B, bias, "ffma", 2)
+    _check_full(got, A, B, bias, "ffma")
+
+
+# Ragged in every dimension; K and N multiples of 8 so that bf16 rows keep
+# 16-byte pitches (the TMA rule).
+SHAPES = [(128, 128, 32), (256, 512, 256), (200, 136, 104), (129, 264, 40), (1, 8, 8),
+          (300, 520, 200), (640, 384, 1000), (383, 776, 1352)]
+
+
+@pytest.mark.parametrize("dtype", ["ffma", "tf32", "bf16"])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_small_shapes(gbr, dtype, M, N, K):
+    A, B, bias = inputs.gemm_uniform(M, N, K, seed=M * 31 + N * 7 + K)
+    if dtype == "bf16":
+        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    got = _run(gbr, A, B, bias, dtype, 2)
+    _check_full(got, A.float(), B.float(), bias, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["ffma", "tf32", "bf16"])
+def test_stage_sweep(gbr, dtype):
+    M, N, K = 384, 512, 640
+    A, B, bias = inputs.gemm_normal(M, N, K, seed=5)
+    if dtype == "bf16":
+        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    smax = gbr.max_stages(gbr.OP_GEMM, {"ffma": 0, "tf32": 1, "bf16": 2}[dtype])
+    assert smax >= 4
+    for S in range(1, smax + 1):
+        got = _run(gbr, A, B, bias, dtype, S)
+        _check_full(got, A.float(), B.float(), bias, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["ffma", "tf32", "bf16"])
+def test_k_zero_is_relu_bias(gbr, dtype):
+    bias = torch.linspace(-2, 2, 264)
+    t = torch.bfloat16 if dtype == "bf16" else torch.float32
+    A = torch.empty((70, 0), dtype=t)
+    B = torch.empty((0, 264), dtype=t)
+    C = gbr.gemm_bias_relu(A.cuda(), B.cuda(), bias.cuda(), dtype=dtype, stages=2)
+    gbr.check_device()
+    expect = oracle.gemm_bias_relu(A.float(), B.float(), bias)
+    if dtype == "bf16":
+        expect = torch.from_numpy(expect).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(to_host_f64(C), expect)
+
+
+def test_bf16_output_rounding(gbr):
+    """The bf16 result is the fp32 result rounded once: with exactly
+    representable small-integer inputs the accumulation is exact, so the output
+    must equal the oracle rounded to bf16."""
+    g = inputs._gen(9)
+    A = torch.randint(-4, 5, (256, 128), generator=g).to(torch.bfloat16)
+    B = torch.randint(-4, 5, (128, 512), generator=g).to(torch.bfloat16)
+    bias = torch.randint(-50, 51, (512,), generator=g).float() * 0.25
+    C = gbr.gemm_bias_relu(A.cuda(), B.cuda(), bias.cuda(), dtype="bf16", stages=3)
+    gbr.check_device()
+    ref = oracle.gemm_bias_relu(A.float(), B.float(), bias)
+    expect = torch.from_numpy(ref).float().to(torch.bfloat16)
+    assert torch.equal(C.cpu(), expect)
+
+
+def test_ffma_integer_inputs_exact(gbr):
+    g = inputs._gen(10)
+    A = torch.randint(-8, 9, (200, 96), generator=g).float()
+    B = torch.randint(-8, 9, (96, 140), generator=g).float()
+    bias = torch.randint(-100, 101, (140,), generator=g).float()
+    C = gbr.gemm_bias_relu(A.cuda(), B.cuda(), bias.cuda(), dtype="ffma", stages=3)
+    gbr.check_device()
+    assert np.array_equal(to_host_f64(C), oracle.gemm_bias_relu(A, B, bias))
+
+
+def test_errors_are_reported(gbr):
+    from mbarrier_gemm_pipelines_gb300 import _binding as b
+    lib = b.lib()
+    A = torch.zeros((64, 64), device="cuda")
+    bias = torch.zeros(64, device="cuda")
+    C = torch.zeros((64, 64), device="cuda")
+    # stages outside [1, max]
+    assert lib.gemm_bias_relu(A.data_ptr(), A.data_ptr(), bias.data_ptr(), C.data_ptr(),
+                              64, 64, 64, 0, 0, None) == b.ERR_SMEM
+    assert lib.gemm_bias_relu(A.data_ptr(), A.data_ptr(), bias.data_ptr(), C.data_ptr(),
+                              64, 64, 64, 2, 9, None) == b.ERR_SMEM
+    # row pitch not a multiple of 16 bytes
+    assert lib.gemm_bias_relu(A.data_ptr(), A.data_ptr(), bias.data_ptr(), C.data_ptr(),
+                              64, 62, 64, 0, 2, None) == b.ERR_ALIGN
+    # misaligned base
+    assert lib.gemm_bias_relu(A.data_ptr() + 4, A.data_ptr(), bias.data_ptr(), C.data_ptr(),
+                              64, 64, 64, 0, 2, None) == b.ERR_ALIGN
+    # C overlapping an input
+    assert lib.gemm_bias_relu(A.data_ptr(), A.data_ptr(), bias.data_ptr(), A.data_ptr(),
+                              64, 64, 64, 0, 2, None) == b.ERR_INVALID
+    assert "overlap" in b.last_error()
+    assert lib.gemm_bias_relu(A.data_ptr(), A.data_ptr(), bias.data_ptr(), C.data_ptr(),
+                              64, 64, 64, 7, 2, None) == b.ERR_INVALID
+    assert "dtype 7" in b.last_error()
+    assert lib.gemm_bias_relu(None, None, None, None, 0, 64, 64, 0, 2, None) == b.OK
+    gbr.check_device()
+
+
+# ------------------------------------------------------------------ full size
+
+def _sampled(gbr, A, B, bias, dtype, stages, npts, seed):
+    d_A, d_B, d_bias = A.cuda(), B.cuda(), bias.cuda()
+    C = gbr.gemm_bias_relu(d_A, d_B, d_bias, dtype=dtype, stages=stages)
+    gbr.check_device()
+    M, N = C.shape
+    ms, ns = sample_points(M, N, npts, seed, extra_rows=(0, M // 2 + 3, M - 1),
+                           extra_cols=(0, N // 3 + 1, N - 1))
+    got = C[torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda()].double().cpu().numpy()
+    ref = oracle.gemm_bias_relu_points(A.float(), B.float(), bias, ms, ns)
+    assert rel_frobenius(got, ref) <= TOL[dtype]
+    # the GEMM part alone (bias-free run) must meet the same bar
+    C0 = gbr.gemm_bias_relu(d_A, d_B, torch.zeros_like(d_bias), dtype=dtype, stages=stages)
+    gbr.check_device()
+    got0 = C0[torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda()].double().cpu().numpy()
+    ref0 = oracle.gemm_bias_relu_points(A.float(), B.float(), torch.zeros_like(bias), ms, ns)
+    assert rel_frobenius(got0, ref0) <= TOL[dtype]
+    return C
+
+
+@pytest.mark.parametrize("dtype,S", [("ffma", 3), ("ffma", 4), ("tf32", 3), ("tf32", 4)])
+def test_config3_fp32_4096(gbr, dtype, S):
+    A, B, bias = inputs.workload("gemm_fp32")
+    _sampled(gbr, A, B, bias, dtype, S, 3000, seed=2)
+
+
+@pytest.mark.parametrize("S", [4])
+def test_config4_bf16_8192(gbr, S):
+    A, B, bias = inputs.workload("gemm_bf16")
+    C = _sampled(gbr, A, B, bias, "bf16", S, 3000, seed=3)
+    assert bool((C >= 0).all())
+
+
+def test_wait_timeout_is_reported_and_context_survives(gbr):
+    gbr.selftest_wait_timeout(50_000_000)   # 50 ms limit on a wait nothing completes
+    assert gbr.device_status() == 6          # GBR_ERR_TIMEOUT
+    assert "timed out" in gbr.last_error()
+    assert gbr.device_status() == 0          # cleared
+    A, B, bias = inputs.gemm_uniform(128, 256, 64, seed=1)
+    got = _run(gbr, A, B, bias, "tf32", 2)
+    _check_full(got, A, B, bias, "tf32")

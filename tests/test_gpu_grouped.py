@@ -1,0 +1,91 @@
+"""Grouped (MoE-style) bf16 GEMM + bias + ReLU in one persistent launch against
+the oracle applied expert by expert.  Bar: relative Frobenius error 1e-2."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mbarrier_gemm_pipelines_gb300 import inputs
+from gpu_helpers import TOL, load_library, rel_frobenius, require_gpu, to_host_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gbr():
+    require_gpu()
+    return load_library()
+
+
+@pytest.mark.parametrize("counts,K,N", [
+    ([130, 0, 7, 256, 1], 192, 520),      # ragged, an empty expert, a one-row expert
+    ([64], 64, 256),
+    ([300, 300, 300], 128, 264),
+    ([0, 0, 129], 72, 512),
+])
+def test_grouped_small(gbr, counts, K, N):
+    G = len(counts)
+    cnt, X, W, b = inputs.grouped(tokens=sum(counts), experts=G, K=K, N=N, seed=sum(counts) + K)
+    cnt = counts                                          # fixed counts for the edge cases
+    C = gbr.gemm_bias_relu_grouped(X.cuda(), W.cuda(), b.cuda(), cnt, stages=3)
+    gbr.check_device()
+    ref = oracle.gemm_bias_relu_grouped(X.float(), W.float(), b, cnt)
+    got = to_host_f64(C)
+    assert rel_frobenius(got, ref) <= TOL["bf16"]
+    assert np.abs(got - ref).max() <= 0.2 * np.abs(ref).max()
+
+
+def test_grouped_matches_dense_per_expert(gbr):
+    """Each expert's rows equal the dense kernel run on that expert alone."""
+    counts = [200, 77, 300]
+    cnt, X, W, b = inputs.grouped(tokens=sum(counts), experts=3, K=256, N=512, seed=11)
+    dX, dW, db = X.cuda(), W.cuda(), b.cuda()
+    C = gbr.gemm_bias_relu_grouped(dX, dW, db, counts, stages=4)
+    off = 0
+    for e, n_e in enumerate(counts):
+        Ce = gbr.gemm_bias_relu(dX[off:off + n_e].contiguous(), dW[e].contiguous(),
+                                db[e].contiguous(), dtype="bf16", stages=4)
+        assert torch.equal(C[off:off + n_e], Ce)
+        off += n_e
+    gbr.check_device()
+
+
+def test_grouped_rejects(gbr):
+    X = torch.zeros((8, 64), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((1, 64, 64), dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros((1, 64), device="cuda")
+    with pytest.raises(ValueError):
+        gbr.gemm_bias_relu_grouped(X, W, b, [9])     # counts must sum to the rows of X
+    from mbarrier_gemm_pipelines_gb300 import _binding as bnd
+    import ctypes
+    cnt = (ctypes.c_int32 * 1)(8)
+    C = torch.zeros((8, 64), device="cuda")
+    assert bnd.lib().gemm_bias_relu_grouped(X.data_ptr(), W.data_ptr(), b.data_ptr(), C.data_ptr(),
+                                            ctypes.cast(cnt, ctypes.c_void_p), 1, 64, 64,
+                                            bnd.F32_FFMA, 2, None) == bnd.ERR_UNSUPPORTED
+    assert bnd.lib().gemm_bias_relu_grouped(X.data_ptr(), W.data_ptr(), b.data_ptr(), C.data_ptr(),
+                                            ctypes.cast(cnt, ctypes.c_void_p), 33, 64, 64,
+                                            bnd.BF16, 2, None) == bnd.ERR_INVALID
+
+
+def test_config5_moe_sampled(gbr):
+    """4096 tokens over 8 experts (Multinomial counts, seed 4), K = 4096,
+    N = 14336, one launch; sampled positions in every expert."""
+    counts, X, W, b = inputs.workload("grouped_bf16")
+    C = gbr.gemm_bias_relu_grouped(X.cuda(), W.cuda(), b.cuda(), counts, stages=4)
+    gbr.check_device()
+    T, N = C.shape
+    rng = np.random.default_rng(4)
+    offs = oracle.group_offsets(counts)
+    rows, cols = [], []
+    for e, n_e in enumerate(counts):
+        if n_e == 0:
+            continue
+        r = offs[e] + rng.integers(0, n_e, 300)
+        rows += list(r) + [offs[e], offs[e] + n_e - 1]
+        cols += list(rng.integers(0, N, 300)) + [0, N - 1]
+    rows = np.array(rows, dtype=np.int64)
+    cols = np.array(cols, dtype=np.int64)
+    got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
+    ref = oracle.gemm_bias_relu_grouped_points(X.float(), W.float(), b, counts, rows, cols)
+    assert rel_frobenius(got, ref) <= TOL["bf16"]
