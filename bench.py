@@ -383,6 +383,38 @@ def run_reference(args):
     emit(res)
 
 
+def run_profile_case(case, launches=2):
+    """A short fixed invocation for Nsight Compute: `launches` launches of one
+    kernel on its workload, nothing timed, nothing printed but a status line."""
+    import torch
+    import mbarrier_gemm_pipelines_gb300 as gbr
+    from mbarrier_gemm_pipelines_gb300 import inputs
+    gbr.build()
+    torch.cuda.set_device(0)
+    if case == "copy":
+        src = inputs.workload("copy").cuda()
+        dst = torch.empty_like(src)
+        fn = lambda: gbr.staged_copy(src, dst, tile=(128, 64), stages=4)
+    elif case in ("gemm_bf16", "gemm_tf32", "gemm_ffma"):
+        if case == "gemm_bf16":
+            A, B, bias = inputs.workload("gemm_bf16")
+        else:
+            A, B, bias = inputs.workload("gemm_fp32")
+        dA, dB, db = A.cuda(), B.cuda(), bias.cuda()
+        dt = case.split("_")[1]
+        fn = lambda: gbr.gemm_bias_relu(dA, dB, db, dtype=dt, stages=4)
+    elif case == "grouped":
+        counts, X, W, b = inputs.workload("grouped_bf16")
+        dX, dW, db = X.cuda(), W.cuda(), b.cuda()
+        fn = lambda: gbr.gemm_bias_relu_grouped(dX, dW, db, counts, stages=4)
+    else:
+        raise SystemExit("unknown profile case %r" % case)
+    for _ in range(launches):
+        fn()
+    gbr.check_device()
+    print("profile case %s: %d launches ok" % (case, launches))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -392,7 +424,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", metavar="CASE",
+                    help="run two launches of one kernel for ncu: copy, gemm_bf16, gemm_tf32, "
+                         "gemm_ffma or grouped")
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args.profile)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
