@@ -174,6 +174,35 @@ int gbr_copy_tuning(int store_lag, int ctas_per_sm);
  */
 int gbr_selftest_wait_timeout(uint64_t timeout_ns, gbr_stream_t stream);
 
+/*
+ * gemm_bias_relu_tf32_noalloc -- the GBR_F32_TF32 case of gemm_bias_relu for
+ * callers that cannot allocate device memory.  It has no counterpart in the
+ * pages; it exists for code that may not call cudaMalloc or cudaMallocAsync:
+ * serving loops that must never enter an allocator (allocation can take locks
+ * or synchronise the device at unpredictable times), plug-ins whose host
+ * framework owns all device allocation, and processes whose device memory is
+ * entirely reserved by another allocator, so that an allocation from this
+ * library would fail.  The TF32 path needs K*N*4 bytes of scratch for a K-major copy of
+ * B plus status words; here both live in one file-scope device array of
+ * 16 MiB + 256 bytes that the CUDA driver creates for every device that loads
+ * this library and keeps until the process exits.  This call allocates nothing.
+ *
+ *   A [M, K], B [K, N], bias [N], C [M, N]: fp32, as for gemm_bias_relu;
+ *   caller-owned device memory.  K and N multiples of 4.
+ *   K * N must be <= 4194304 (K*N*4 bytes <= 16 MiB): larger sizes return
+ *   GBR_ERR_INVALID without launching anything.
+ *   stages, stream: as for gemm_bias_relu.
+ * The first call on a device looks up the array's device address (once, with
+ * that device current); make that first call before any stream capture.
+ * Every call uses the same array: calls that may overlap on the GPU (different
+ * streams, or several devices' work racing on one array) race and give
+ * undefined results -- serialise them.  Each call clears the status words
+ * before use; gbr_device_status() reports a wait timeout recorded there.
+ */
+int gemm_bias_relu_tf32_noalloc(const float *A, const float *B, const float *bias, float *C,
+                                int64_t M, int64_t N, int64_t K, int stages,
+                                gbr_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -35,6 +35,7 @@ SIGNATURES = {
     "gbr_set_wait_timeout_ns": (_i32, [_u64]),
     "gbr_copy_tuning": (_i32, [_i32, _i32]),
     "gbr_selftest_wait_timeout": (_i32, [_u64, _vp]),
+    "gemm_bias_relu_tf32_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
 }
 
 _lib = None
@@ -200,3 +201,22 @@ def copy_tuning(store_lag: int = -1, ctas_per_sm: int = -1) -> None:
 
 def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
     check(lib().gbr_selftest_wait_timeout(int(timeout_ns), _stream_ptr(stream)))
+
+
+def gemm_bias_relu_tf32_noalloc(A, B, bias, C, stages=4, stream=None):
+    """TF32 C = ReLU(A @ B + bias) that allocates no device memory (C is required).
+
+    For callers that may not allocate: serving loops that must stay out of
+    allocators, plug-ins whose host framework owns all device allocation,
+    processes whose device memory is reserved by another allocator.  Scratch comes from a fixed 16 MiB device
+    array shared by all calls (K * N <= 4194304); calls that overlap on the GPU
+    race, so serialise them."""
+    import torch
+    for t, n in ((A, "A"), (B, "B"), (bias, "bias"), (C, "C")):
+        _cuda_tensor(t, n, (torch.float32,))
+    M, K = A.shape
+    N = B.shape[1]
+    check(lib().gemm_bias_relu_tf32_noalloc(A.data_ptr(), B.data_ptr(), bias.data_ptr(),
+                                            C.data_ptr(), M, N, K, int(stages),
+                                            _stream_ptr(stream)))
+    return C

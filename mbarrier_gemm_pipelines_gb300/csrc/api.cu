@@ -193,6 +193,11 @@ int check_umma_regs(DevCtx& c, int kind, bool grouped) {
 }
 
 }  // namespace
+
+int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+void count_launch() { ++g_launches; }
+uint64_t wait_timeout_ns() { return timeout_ns(); }
+
 }  // namespace gbr
 
 using namespace gbr;
@@ -250,7 +255,15 @@ int gbr_device_status(gbr_stream_t stream) {
     uint32_t st[kStatusWords];
     if ((e = cudaMemcpy(st, c->status, sizeof(st), cudaMemcpyDeviceToHost)) != cudaSuccess)
         return cuda_fail(e, "reading the status block");
-    if (st[0] == 0) return GBR_OK;
+    if (st[0] == 0) {
+        // Calls of gemm_bias_relu_tf32_noalloc record into their own scratch array.
+        uint32_t na[4] = {0, 0, 0, 0};
+        if (noalloc_take_status(na) == 0) return GBR_OK;
+        return fail(GBR_ERR_TIMEOUT,
+                    "a pipeline wait of gemm_bias_relu_tf32_noalloc timed out (site 0x%02x, CTA "
+                    "%u, item %u); that call's output is undefined",
+                    na[1], na[2], na[3]);
+    }
     if ((e = cudaMemset(c->status, 0, sizeof(st))) != cudaSuccess)
         return cuda_fail(e, "clearing the status block");
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");

@@ -83,6 +83,16 @@ cudaError_t launch_gemm_umma_grouped(const CUtensorMap& mapX, const CUtensorMap&
 // Bt[N, K] = B[K, N], 32-bit elements, K and N multiples of 4.
 cudaError_t launch_transpose_f32(const float* B, float* Bt, int K, int N, cudaStream_t stream);
 
+// ------------------------------------------------------------ no-alloc variant
+// Status words of the no-alloc scratch on the current device: returns the error
+// bits (0: none or never set up) and copies words [0..3] out, then clears them.
+uint32_t noalloc_take_status(uint32_t* words4);
+
+// ------------------------------------------------------------ api.cu services
+int report_error(int code, const char* msg);   // sets gbr_last_error(), returns code
+void count_launch();                           // adds one to gbr_launch_count()
+uint64_t wait_timeout_ns();                    // current per-wait limit
+
 // ------------------------------------------------------------ self test
 cudaError_t launch_wait_selftest(KernelCtl ctl, cudaStream_t stream);
 

@@ -1,0 +1,205 @@
+// noalloc.cu -- the TF32 GEMM + bias + ReLU for callers that cannot allocate
+// device memory.
+//
+// The regular TF32 entry point needs K*N*4 bytes of scratch for the K-major
+// copy of B, which it takes from the stream-ordered allocator on every call,
+// plus the library's per-device status block, which it allocates on first use.
+// Some callers cannot do either: serving loops that must never enter an
+// allocator (it can take locks or synchronise the device at unpredictable
+// times), plug-ins whose host framework owns all device allocation, and
+// processes whose device memory is entirely reserved by another allocator, so
+// that a cudaMalloc or cudaMallocAsync from this library would fail.  This
+// variant runs the same two kernels (B transpose, then the tcgen05 TF32 GEMM)
+// but takes all its scratch -- status words and the transposed B -- from one
+// file-scope device array that the CUDA driver creates when the library's
+// module is loaded.
+#include "gbr.h"
+#include "gbr_internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+namespace gbr {
+
+namespace {
+
+constexpr size_t kNoallocStatusBytes = 256;             // kStatusWords words, padded
+constexpr size_t kNoallocBtBytes = size_t(16) << 20;    // largest K*N*4 accepted
+constexpr size_t kNoallocScratchBytes = kNoallocStatusBytes + kNoallocBtBytes;
+
+// Held by every device that loads this library until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+constexpr int kMaxDev = 64;
+struct NoallocDevice {
+    bool ready = false;
+    unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch
+    int sm_count = 0;
+    int smem_optin = 0;
+    bool regs_ok = false;
+};
+NoallocDevice g_na[kMaxDev];
+std::mutex g_na_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 na_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool na_map_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
+               uint32_t box_inner, uint32_t box_outer) {
+    auto fn = na_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 4};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Once per device, with that device current: the device address of the
+// scratch array (in host code the array's name is only a host-side stand-in),
+// the attributes the launch needs, and the register check of the GEMM kernel.
+int na_setup(NoallocDevice** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return report_error(GBR_ERR_CUDA, "cudaGetDevice failed");
+    if (dev < 0 || dev >= kMaxDev) return report_error(GBR_ERR_INVALID, "device index out of range");
+    std::lock_guard<std::mutex> lk(g_na_mu);
+    NoallocDevice& d = g_na[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
+            return report_error(GBR_ERR_CUDA, "cudaDeviceGetAttribute failed");
+        if (major != 10 || minor != 3)
+            return report_error(GBR_ERR_UNSUPPORTED, "this library is built for sm_103a only");
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return report_error(GBR_ERR_CUDA, "cudaGetSymbolAddress(no-alloc scratch) failed");
+        int regs = 0;
+        d.regs_ok = umma_check_registers(kUmmaTf32, false, &regs) == cudaSuccess;
+        d.scratch = static_cast<unsigned char*>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return GBR_OK;
+}
+
+}  // namespace
+
+// Reads and clears the status words of the no-alloc scratch on the current
+// device; 0 if nothing was recorded or the scratch was never set up there.
+uint32_t noalloc_take_status(uint32_t* words4) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    unsigned char* scratch;
+    {
+        std::lock_guard<std::mutex> lk(g_na_mu);
+        if (!g_na[dev].ready) return 0;
+        scratch = g_na[dev].scratch;
+    }
+    uint32_t st[kStatusWords];
+    if (cudaMemcpy(st, scratch, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return 0;
+    if (st[0] == 0) return 0;
+    cudaMemset(scratch, 0, sizeof(st));
+    for (int i = 0; i < 4; ++i) words4[i] = st[i];
+    return st[0];
+}
+
+}  // namespace gbr
+
+using namespace gbr;
+
+extern "C" int gemm_bias_relu_tf32_noalloc(const float* A, const float* B, const float* bias,
+                                           float* C, int64_t M, int64_t N, int64_t K, int stages,
+                                           gbr_stream_t stream) {
+    const int64_t lim = int64_t(1) << 31;
+    if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim)
+        return report_error(GBR_ERR_INVALID, "gemm_bias_relu_tf32_noalloc: M, N, K must be in [0, 2^31)");
+    if (uint64_t(K) * uint64_t(N) * 4u > kNoallocBtBytes)
+        return report_error(GBR_ERR_INVALID,
+                            "gemm_bias_relu_tf32_noalloc: K*N*4 bytes exceeds the 16 MiB no-alloc "
+                            "scratch (K*N must be <= 4194304); use gemm_bias_relu");
+    NoallocDevice* d;
+    int r = na_setup(&d);
+    if (r != GBR_OK) return r;
+    const size_t ring_bytes = 1024 + size_t(stages) * kUmmaStageBytes + kUmmaEpiBytes + 256;
+    if (stages < 1 || ring_bytes > size_t(d->smem_optin))
+        return report_error(GBR_ERR_SMEM, "gemm_bias_relu_tf32_noalloc: stages out of range");
+    if (M == 0 || N == 0) return GBR_OK;
+    if (!C || !bias || (K > 0 && (!A || !B)))
+        return report_error(GBR_ERR_INVALID, "gemm_bias_relu_tf32_noalloc: NULL buffer");
+    auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!al(C) || !al(bias) || (K > 0 && (!al(A) || !al(B))) || (N % 4) || (K % 4))
+        return report_error(GBR_ERR_ALIGN,
+                            "gemm_bias_relu_tf32_noalloc: 16-byte aligned buffers, K and N "
+                            "multiples of 4");
+    if (!d->regs_ok)
+        return report_error(GBR_ERR_CUDA, "tcgen05 GEMM kernel has too few registers for its role split");
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t* status = reinterpret_cast<uint32_t*>(d->scratch);
+    float* bt = reinterpret_cast<float*>(d->scratch + kNoallocStatusBytes);
+    // The array keeps the last call's contents; the status words must start at zero.
+    if (cudaMemsetAsync(status, 0, kNoallocStatusBytes, st) != cudaSuccess)
+        return report_error(GBR_ERR_CUDA, "clearing the no-alloc status words failed");
+
+    GemmShape s;
+    memset(&s, 0, sizeof(s));
+    s.M = int32_t(M);
+    s.N = int32_t(N);
+    s.K = int32_t(K);
+    s.stages = stages;
+    s.bias = bias;
+    s.C = C;
+    s.ctl.status = status;
+    s.ctl.timeout_ns = wait_timeout_ns();
+    s.m_tiles = int32_t((M + kUmmaBM - 1) / kUmmaBM);
+    s.n_tiles = int32_t((N + kUmmaBN - 1) / kUmmaBN);
+    s.num_kb = int32_t((K + 31) / 32);
+    s.num_tiles = s.m_tiles * s.n_tiles;
+    s.group_m = 16;
+    CUtensorMap ma, mb, mc;
+    if (!na_map_2d(&mc, C, uint64_t(N), uint64_t(M), 32, 32))
+        return report_error(GBR_ERR_INVALID, "encoding the C tensor map failed");
+    if (K > 0) {
+        if (!na_map_2d(&ma, A, uint64_t(K), uint64_t(M), 32, 128) ||
+            !na_map_2d(&mb, bt, uint64_t(K), uint64_t(N), 32, 256))
+            return report_error(GBR_ERR_INVALID, "encoding the A/B tensor maps failed");
+    } else {
+        ma = mc;
+        mb = mc;
+    }
+    const size_t smem = umma_smem_bytes(stages);
+    if (umma_prepare(kUmmaTf32, false, smem) != cudaSuccess)
+        return report_error(GBR_ERR_CUDA, "cudaFuncSetAttribute(tcgen05 GEMM) failed");
+    if (K > 0) {
+        if (launch_transpose_f32(B, bt, int(K), int(N), st) != cudaSuccess)
+            return report_error(GBR_ERR_CUDA, "launching the B transpose failed");
+        count_launch();
+    }
+    const int grid = int(std::min<int64_t>(s.num_tiles, d->sm_count));
+    if (launch_gemm_umma(kUmmaTf32, ma, mb, mc, s, grid, smem, st) != cudaSuccess)
+        return report_error(GBR_ERR_CUDA, "launching the tcgen05 GEMM failed");
+    count_launch();
+    return GBR_OK;
+}
