@@ -246,6 +246,57 @@ def measure_copy(gbr, peaks, stages=4, steps=40, warmup=5):
     }
 
 
+def measure_workloads(gbr, peaks, sm_mhz=None, steps=20, warmup=3):
+    """The other GEMM workloads, each against the roofline of its own unit."""
+    import torch
+    from mbarrier_gemm_pipelines_gb300 import inputs
+    stream = torch.cuda.current_stream()
+    bf16_peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    clock_ghz = (sm_mhz or peaks.get("sm_max_mhz", 2070.0)) / 1e3
+    fp32_alu_peak = 152 * 128 * 2 * clock_ghz / 1e3          # TFLOP/s
+    out = {}
+
+    def timed(fn, flops):
+        for _ in range(warmup):
+            fn()
+        t = time_launches(fn, steps, stream)
+        gbr.check_device()
+        return flops * steps / t / 1e12, t / steps * 1e3
+
+    A, B, bias = inputs.workload("gemm_fp32")
+    dA, dB, db = A.cuda(), B.cuda(), bias.cuda()
+    dC = torch.empty((4096, 4096), device="cuda")
+    f = gemm_flops(4096, 4096, 4096)
+    for dt, peak, bound, unit in (("ffma", fp32_alu_peak, "alu", "FP32 FMA lanes: 152 SM x 128 x 2 x f_SM"),
+                                  ("tf32", bf16_peak * 0.5, "tensor",
+                                   "measured bf16 x 0.5 (nominal TF32:bf16 dense ratio)")):
+        for S in (3, 4):
+            v, ms = timed(lambda: gbr.gemm_bias_relu(dA, dB, db, dC, dtype=dt, stages=S), f)
+            out["gemm_fp32_4096_%s_S%d" % (dt, S)] = {
+                "value": round(v, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
+                "roofline": {"bound": bound, "achieved": round(v, 2), "peak": round(peak, 1),
+                             "unit": "TFLOP/s", "frac": round(v / peak, 4), "peak_note": unit}}
+    del dA, dB, db, dC
+    A, B, bias = inputs.workload("gemm_small")
+    dA, dB, db = A.cuda(), B.cuda(), bias.cuda()
+    dC = torch.empty((256, 256), device="cuda")
+    v, ms = timed(lambda: gbr.gemm_bias_relu(dA, dB, db, dC, dtype="ffma", stages=2),
+                  gemm_flops(256, 256, 256))
+    out["gemm_fp32_256_ffma_S2"] = {"value": round(v, 3), "unit": "TFLOP/s",
+                                    "us_per_call": round(ms * 1e3, 2),
+                                    "note": "4 CTAs of 128x128: launch/latency-bound"}
+    counts, X, W, b = inputs.workload("grouped_bf16")
+    dX, dW, db = X.cuda(), W.cuda(), b.cuda()
+    dC = torch.empty((sum(counts), W.shape[2]), dtype=torch.bfloat16, device="cuda")
+    f = 2.0 * sum(counts) * W.shape[1] * W.shape[2]
+    v, ms = timed(lambda: gbr.gemm_bias_relu_grouped(dX, dW, db, counts, dC, stages=4), f)
+    out["grouped_bf16_moe_S4"] = {
+        "value": round(v, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4), "counts": counts,
+        "roofline": {"bound": "tensor", "achieved": round(v, 2), "peak": bf16_peak,
+                     "unit": "TFLOP/s", "frac": round(v / bf16_peak, 4)}}
+    return out
+
+
 def run_ours(args):
     import torch
     import mbarrier_gemm_pipelines_gb300 as gbr
@@ -305,6 +356,9 @@ def run_ours(args):
     d2h = hC.numel() * 2
 
     copy = measure_copy(gbr, peaks) if rank == 0 else None
+    others = None
+    if rank == 0 and not args.quick:
+        others = measure_workloads(gbr, peaks, sm_mhz=(clocks or {}).get("sm_mhz"))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -342,6 +396,7 @@ def run_ours(args):
         "clocks": clocks,
         "cpu_baseline": cpu,
         "staged_copy": copy,
+        "other_workloads": others,
     }
     emit(res)
 
@@ -424,6 +479,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="skip the secondary workloads (fp32 4096^3, 256^3, grouped MoE)")
     ap.add_argument("--profile", metavar="CASE",
                     help="run two launches of one kernel for ncu: copy, gemm_bf16, gemm_tf32, "
                          "gemm_ffma or grouped")
