@@ -76,7 +76,8 @@ typedef enum {
  *   dtype gbr_dtype.
  *   stages  ring depth S, 1 <= S <= gbr_max_stages(GBR_OP_GEMM, dtype, 0, 0)
  *         (GBR_ERR_SMEM otherwise).  Tiles: FFMA 128x128x32 fp32;
- *         tcgen05 128x256 with 128 bytes of K per stage (bf16 K=64, tf32 K=32).
+ *         tcgen05 128x256 per CTA, or 256x256 per CTA pair (gbr_gemm_tuning),
+ *         with 128 bytes of K per stage (bf16 K=64, tf32 K=32).
  *   stream  see above.
  * Ragged M, N and K need no padding: TMA loads zero-fill outside the tensor
  * and TMA stores drop rows/columns outside it.
@@ -144,8 +145,9 @@ const char *gbr_last_error(void);
 enum { GBR_OP_GEMM = 0, GBR_OP_COPY = 1 };
 
 /* Largest ring depth that fits the current device's per-CTA shared memory:
- * op GBR_OP_GEMM uses `dtype`; GBR_OP_COPY uses tile_rows x tile_cols fp32.
- * Returns a negative gbr_status on error. */
+ * op GBR_OP_GEMM uses `dtype` (tensor-core dtypes: the CTA-pair kernel's
+ * limit; one CTA per tile holds 4); GBR_OP_COPY uses tile_rows x tile_cols
+ * fp32.  Returns a negative gbr_status on error. */
 int gbr_max_stages(int op, int dtype, int tile_rows, int tile_cols);
 
 /* Number of kernels this library has launched in this process. */
@@ -165,6 +167,16 @@ int gbr_set_wait_timeout_ns(uint64_t ns);
  * as shared memory allows), else 1..occupancy.
  */
 int gbr_copy_tuning(int store_lag, int ctas_per_sm);
+
+/*
+ * Tensor-core GEMM tuning, process-wide (gemm_bias_relu with GBR_BF16 or
+ * GBR_F32_TF32, and gemm_bias_relu_grouped).  cta_pair: -1 auto, 1 (one CTA
+ * per 128x256 output tile, S <= 4), 2 (a two-CTA cluster per 256x256 tile,
+ * cta_group::2 MMA, S <= 6).  Auto picks 2 when there is more than one
+ * 128-row tile or S > 4 (grouped: when 256-row tiles waste at most ~10% more
+ * rows).  group_m: -1 auto, else output-tile rows per raster band.
+ */
+int gbr_gemm_tuning(int cta_pair, int group_m);
 
 /*
  * Failure-detection self test: launches one CTA that waits, with the given

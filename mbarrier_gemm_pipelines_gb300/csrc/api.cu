@@ -23,6 +23,8 @@ std::mutex g_mu;
 uint64_t g_timeout_ns = 0;  // 0: not yet resolved
 int g_copy_store_lag = -1;
 int g_copy_ctas_per_sm = -1;
+int g_gemm_pair = -1;      // -1 auto, 1 one CTA per tile, 2 CTA pair per tile
+int g_gemm_group_m = -1;   // -1 auto: tile rows per raster band
 
 constexpr int kMaxDevices = 64;
 
@@ -32,8 +34,8 @@ struct DevCtx {
     int smem_optin = 0;
     uint32_t* status = nullptr;
     bool ffma_regs_ok = false, ffma_regs_checked = false;
-    bool umma_regs_ok[2][2] = {{false, false}, {false, false}};
-    bool umma_regs_checked[2][2] = {{false, false}, {false, false}};
+    bool umma_regs_ok[2][2][2] = {};        // [kind][grouped][pair - 1]
+    bool umma_regs_checked[2][2][2] = {};
 };
 DevCtx g_dev[kMaxDevices];
 
@@ -160,14 +162,46 @@ int max_stages_for(size_t (*bytes)(int), int smem_optin) {
 }
 
 size_t ffma_bytes_fn(int s) { return ffma_smem_bytes(s); }
-size_t umma_bytes_fn(int s) {
-    // The padding that keeps one CTA per SM is not part of the ring budget.
-    return 1024 + size_t(s) * kUmmaStageBytes + kUmmaEpiBytes + 256;
+// The padding that keeps one CTA per SM is not part of the ring budget.
+size_t umma1_bytes_fn(int s) { return umma_ring_bytes(s, 1); }
+size_t umma2_bytes_fn(int s) { return umma_ring_bytes(s, 2); }
+
+int umma_max_stages(int pair, int smem_optin) {
+    return max_stages_for(pair == 2 ? umma2_bytes_fn : umma1_bytes_fn, smem_optin);
 }
 
+// Largest ring depth for the dtype (tcgen05: that of the CTA-pair kernel).
 int gemm_max_stages(int dtype, int smem_optin) {
     return dtype == GBR_F32_FFMA ? max_stages_for(ffma_bytes_fn, smem_optin)
-                                 : max_stages_for(umma_bytes_fn, smem_optin);
+                                 : umma_max_stages(2, smem_optin);
+}
+
+// One CTA or a CTA pair per tile: forced by gbr_gemm_tuning, else the pair
+// whenever there is more than one 128-row tile or the ring is deeper than the
+// one-CTA kernel can hold.
+int choose_pair(int64_t rows, int stages, int smem_optin, int* pair) {
+    int forced;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        forced = g_gemm_pair;
+    }
+    const int max1 = umma_max_stages(1, smem_optin);
+    if (forced == 1) {
+        if (stages > max1)
+            return fail(GBR_ERR_SMEM, "stages=%d exceeds %d for one CTA per tile", stages, max1);
+        *pair = 1;
+    } else if (forced == 2) {
+        *pair = 2;
+    } else {
+        *pair = (rows > 128 || stages > max1) ? 2 : 1;
+    }
+    return GBR_OK;
+}
+
+int group_m_for(int pair) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_gemm_group_m > 0) return g_gemm_group_m;
+    return pair == 2 ? 8 : 16;
 }
 
 int copy_max_stages(uint32_t tile_bytes, int smem_optin) {
@@ -176,17 +210,17 @@ int copy_max_stages(uint32_t tile_bytes, int smem_optin) {
     return s;
 }
 
-int check_umma_regs(DevCtx& c, int kind, bool grouped) {
+int check_umma_regs(DevCtx& c, int kind, bool grouped, int pair) {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!c.umma_regs_checked[kind][grouped]) {
+    if (!c.umma_regs_checked[kind][grouped][pair - 1]) {
         int regs = 0;
-        cudaError_t e = umma_check_registers(kind, grouped, &regs);
-        c.umma_regs_checked[kind][grouped] = true;
-        c.umma_regs_ok[kind][grouped] = (e == cudaSuccess);
+        cudaError_t e = umma_check_registers(kind, grouped, pair, &regs);
+        c.umma_regs_checked[kind][grouped][pair - 1] = true;
+        c.umma_regs_ok[kind][grouped][pair - 1] = (e == cudaSuccess);
         if (e != cudaSuccess && e != cudaErrorInvalidConfiguration)
             return cuda_fail(e, "cudaFuncGetAttributes(tcgen05 GEMM)");
     }
-    if (!c.umma_regs_ok[kind][grouped])
+    if (!c.umma_regs_ok[kind][grouped][pair - 1])
         return fail(GBR_ERR_CUDA,
                     "tcgen05 GEMM kernel was built with too few registers for its role split");
     return GBR_OK;
@@ -227,6 +261,15 @@ int gbr_copy_tuning(int store_lag, int ctas_per_sm) {
     std::lock_guard<std::mutex> lk(g_mu);
     g_copy_store_lag = store_lag;
     g_copy_ctas_per_sm = ctas_per_sm;
+    return GBR_OK;
+}
+
+int gbr_gemm_tuning(int cta_pair, int group_m) {
+    if (!(cta_pair == -1 || cta_pair == 1 || cta_pair == 2) || group_m == 0 || group_m < -1)
+        return fail(GBR_ERR_INVALID, "gbr_gemm_tuning: cta_pair in {-1,1,2}, group_m -1 or >= 1");
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_gemm_pair = cta_pair;
+    g_gemm_group_m = group_m;
     return GBR_OK;
 }
 
@@ -442,20 +485,22 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
         dtype == GBR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const uint32_t bk = uint32_t(128 / es);          // K per stage
     const uint32_t panel_cols = uint32_t(128 / es);  // B panel width; also the C store box width
-    s.m_tiles = int32_t(cdiv(M, kUmmaBM));
+    int pair = 1;
+    if ((r = choose_pair(M, stages, c->smem_optin, &pair)) != GBR_OK) return r;
+    s.m_tiles = int32_t(cdiv(M, int64_t(kUmmaBM) * pair));
     s.n_tiles = int32_t(cdiv(N, kUmmaBN));
     s.num_kb = int32_t(cdiv(K, bk));
     s.num_tiles = s.m_tiles * s.n_tiles;
-    s.group_m = 16;
+    s.group_m = group_m_for(pair);
     CUtensorMap ma, mb, mc;
     if ((r = encode_2d(&mc, dt, C, uint64_t(N), uint64_t(M), uint64_t(N) * es, panel_cols, 32,
                        CU_TENSOR_MAP_SWIZZLE_128B, "C")) != GBR_OK)
         return r;
-    if ((r = check_umma_regs(*c, kind, false)) != GBR_OK) return r;
-    const size_t smem = umma_smem_bytes(stages);
-    if ((e = umma_prepare(kind, false, smem)) != cudaSuccess)
+    if ((r = check_umma_regs(*c, kind, false, pair)) != GBR_OK) return r;
+    const size_t smem = umma_smem_bytes(stages, pair);
+    if ((e = umma_prepare(kind, false, pair, smem)) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(tcgen05 GEMM)");
-    const int grid = int(std::min<int64_t>(s.num_tiles, c->sm_count));
+    const int grid = pair * int(std::min<int64_t>(s.num_tiles, c->sm_count / pair));
     float* bt = nullptr;  // TF32 only: K-major copy of B, stream-ordered scratch
     if (K > 0) {
         if ((r = encode_2d(&ma, dt, A, uint64_t(K), uint64_t(M), uint64_t(K) * es, bk, 128,
@@ -469,8 +514,9 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
             if ((e = cudaMallocAsync(reinterpret_cast<void**>(&bt), size_t(K) * size_t(N) * 4, st)) !=
                 cudaSuccess)
                 return cuda_fail(e, "cudaMallocAsync(TF32 B transpose)");
-            if ((r = encode_2d(&mb, dt, bt, uint64_t(K), uint64_t(N), uint64_t(K) * es, bk, 256,
-                               CU_TENSOR_MAP_SWIZZLE_128B, "Bt")) != GBR_OK) {
+            if ((r = encode_2d(&mb, dt, bt, uint64_t(K), uint64_t(N), uint64_t(K) * es, bk,
+                               uint32_t(kUmmaBN / pair), CU_TENSOR_MAP_SWIZZLE_128B,
+                               "Bt")) != GBR_OK) {
                 cudaFreeAsync(bt, st);
                 return r;
             }
@@ -485,7 +531,7 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
         ma = mc;  // never read: no k-blocks are loaded when K == 0
         mb = mc;
     }
-    e = launch_gemm_umma(kind, ma, mb, mc, s, grid, smem, st);
+    e = launch_gemm_umma(kind, pair, ma, mb, mc, s, grid, smem, st);
     if (bt) cudaFreeAsync(bt, st);
     if (e != cudaSuccess) return cuda_fail(e, "launching tcgen05 GEMM");
     ++g_launches;
@@ -540,7 +586,30 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
     s.ctl = make_ctl(*c);
     s.n_tiles = int32_t(cdiv(N, kUmmaBN));
     s.num_kb = int32_t(cdiv(K, 64));
-    s.group_m = 16;
+    int pair = 1;
+    {
+        // Auto: the pair when its 256-row tiles waste at most ~10% more rows
+        // than 128-row tiles over the experts' row counts.
+        int64_t rows1 = 0, rows2 = 0, maxn = 0;
+        for (int e2 = 0; e2 < num_groups; ++e2) {
+            rows1 += cdiv(counts_host[e2], 128) * 128;
+            rows2 += cdiv(counts_host[e2], 256) * 256;
+            maxn = std::max<int64_t>(maxn, counts_host[e2]);
+        }
+        int forced;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            forced = g_gemm_pair;
+        }
+        const int max1 = umma_max_stages(1, c->smem_optin);
+        if (forced == 1 && stages > max1)
+            return fail(GBR_ERR_SMEM, "stages=%d exceeds %d for one CTA per tile", stages, max1);
+        if (forced > 0)
+            pair = forced;
+        else
+            pair = (stages > max1 || (maxn > 128 && rows2 * 10 <= rows1 * 11)) ? 2 : 1;
+    }
+    s.group_m = group_m_for(pair);
     GroupTable g;
     memset(&g, 0, sizeof(g));
     g.num_groups = num_groups;
@@ -551,7 +620,7 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
         const int64_t n_e = counts_host[e];
         g.row_off[e] = int32_t(off);
         g.rows[e] = int32_t(n_e);
-        g.m_tiles[e] = int32_t(cdiv(n_e, kUmmaBM));
+        g.m_tiles[e] = int32_t(cdiv(n_e, int64_t(kUmmaBM) * pair));
         g.tile_start[e] = int32_t(tiles);
         tiles += int64_t(g.m_tiles[e]) * s.n_tiles;
         if (n_e > 0) {
@@ -584,12 +653,12 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
         mx = mc[last_valid];
         mw = mc[last_valid];
     }
-    if ((r = check_umma_regs(*c, kUmmaBf16, true)) != GBR_OK) return r;
-    const size_t smem = umma_smem_bytes(stages);
-    cudaError_t e = umma_prepare(kUmmaBf16, true, smem);
+    if ((r = check_umma_regs(*c, kUmmaBf16, true, pair)) != GBR_OK) return r;
+    const size_t smem = umma_smem_bytes(stages, pair);
+    cudaError_t e = umma_prepare(kUmmaBf16, true, pair, smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(grouped GEMM)");
-    const int grid = int(std::min<int64_t>(s.num_tiles, c->sm_count));
-    if ((e = launch_gemm_umma_grouped(mx, mw, mc, g, s, int64_t(N), grid, smem,
+    const int grid = pair * int(std::min<int64_t>(s.num_tiles, c->sm_count / pair));
+    if ((e = launch_gemm_umma_grouped(pair, mx, mw, mc, g, s, int64_t(N), grid, smem,
                                       reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
         return cuda_fail(e, "launching grouped GEMM");
     ++g_launches;

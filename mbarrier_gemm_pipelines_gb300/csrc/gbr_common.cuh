@@ -41,15 +41,23 @@ __device__ __forceinline__ void record_timeout(const KernelCtl& ctl, uint32_t si
     }
 }
 
+// One poll of a barrier phase; CLUSTER selects cluster-scope acquire, for
+// barriers that receive arrivals or commits from the other CTA of a pair.
+template <bool CLUSTER>
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
+    return CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+}
+
 // Slow path of a bounded wait: polls until the phase completes, another role
 // raised the CTA's abort flag, or the time/iteration limit runs out (then it
 // records the site, raises the abort flag and gives up).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
-                                            volatile int* abort_flag, uint32_t site,
-                                            uint32_t item) {
+                                               volatile int* abort_flag, uint32_t site,
+                                               uint32_t item) {
     const uint64_t t0 = ptx::globaltimer();
     for (uint32_t iter = 0; iter < kMaxPollIters; ++iter) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (mbar_poll<CLUSTER>(bar, parity)) return true;
         if (*abort_flag) return false;
         if (ptx::globaltimer() - t0 > ctl.timeout_ns) break;
     }
@@ -59,19 +67,21 @@ __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, co
 }
 
 // Bounded wait for the phase of `bar` with the given parity to complete.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
                                           volatile int* abort_flag, uint32_t site, uint32_t item) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, ctl, abort_flag, site, item);
+    if (mbar_poll<CLUSTER>(bar, parity)) return true;
+    return mbar_wait_slow<CLUSTER>(bar, parity, ctl, abort_flag, site, item);
 }
 
 // The same wait taken by all 32 lanes of a warp.  The outcome is made
 // warp-uniform, so a warp never splits into lanes that carry on and lanes that
 // abort (the warp-wide .sync.aligned instructions that follow need every lane).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
                                                volatile int* abort_flag, uint32_t site,
                                                uint32_t item) {
-    const bool ok = mbar_wait(bar, parity, ctl, abort_flag, site, item);
+    const bool ok = mbar_wait<CLUSTER>(bar, parity, ctl, abort_flag, site, item);
     return __all_sync(0xffffffffu, ok);
 }
 

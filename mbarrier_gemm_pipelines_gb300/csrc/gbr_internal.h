@@ -65,17 +65,26 @@ struct GroupTable {
     int32_t num_groups;
     int32_t row_off[kMaxGroups];       // first row of group e in X and C
     int32_t rows[kMaxGroups];          // n_e
-    int32_t m_tiles[kMaxGroups];       // ceil(n_e / 128)
+    int32_t m_tiles[kMaxGroups];       // ceil(n_e / tile rows)
     int32_t tile_start[kMaxGroups + 1];  // prefix sum of m_tiles[e] * n_tiles
 };
 
+// pair = 1: one CTA per 128x256 tile; pair = 2: a two-CTA cluster per 256x256
+// tile (cta_group::2).  Overloads without `pair` mean pair = 1.
+size_t umma_ring_bytes(int stages, int pair);    // shared memory the ring needs
+size_t umma_smem_bytes(int stages, int pair);    // what the launch requests
 size_t umma_smem_bytes(int stages);
+cudaError_t umma_prepare(int kind, bool grouped, int pair, size_t smem);
 cudaError_t umma_prepare(int kind, bool grouped, size_t smem);
+cudaError_t umma_check_registers(int kind, bool grouped, int pair, int* regs);
 cudaError_t umma_check_registers(int kind, bool grouped, int* regs);
+cudaError_t launch_gemm_umma(int kind, int pair, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                             const CUtensorMap& mapC, const GemmShape& s, int grid, size_t smem,
+                             cudaStream_t stream);
 cudaError_t launch_gemm_umma(int kind, const CUtensorMap& mapA, const CUtensorMap& mapB,
                              const CUtensorMap& mapC, const GemmShape& s, int grid, size_t smem,
                              cudaStream_t stream);
-cudaError_t launch_gemm_umma_grouped(const CUtensorMap& mapX, const CUtensorMap& mapW,
+cudaError_t launch_gemm_umma_grouped(int pair, const CUtensorMap& mapX, const CUtensorMap& mapW,
                                      const CUtensorMap* mapsC, const GroupTable& g,
                                      const GemmShape& s, int64_t bias_group_stride, int grid,
                                      size_t smem, cudaStream_t stream);

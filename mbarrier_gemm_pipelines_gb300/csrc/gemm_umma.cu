@@ -1,5 +1,6 @@
 // gemm_umma.cu -- warp-specialized, persistent tensor-core GEMM + bias + ReLU
-// for sm_103a (tcgen05 MMA into Tensor Memory), bf16 or TF32 inputs.
+// for sm_103a (tcgen05 MMA into Tensor Memory), bf16 or TF32 inputs, one CTA
+// per output tile (PAIR = 1) or a CTA pair per tile (PAIR = 2).
 //
 // Method ("gpu_warp_specialization", "The architecture: every piece
 // explained" and "End-to-end flow"; "pwwt.cn news/4436243", sections 3.2-3.4
@@ -22,19 +23,33 @@
 //     second 2-slot ring with the same slot/parity rule.
 //   * Epilogue: tcgen05.ld -> +bias -> ReLU -> (bf16 round-to-nearest-even)
 //     -> 128-byte swizzled st.shared -> TMA store, per warp, double-buffered.
-//   * Persistent CTAs (one per SM) walk tiles t = blockIdx.x + j * gridDim.x
-//     in banded order; every role walks the same sequence, and the
-//     k-iteration counter runs across tiles so phases carry over.
+//   * Persistent CTAs walk tiles t = unit + j * units in banded order; every
+//     role walks the same sequence, and the k-iteration counter runs across
+//     tiles so phases carry over.
 //   * Registers move from warpgroup 0 (producer / MMA / TMEM allocator) to the
 //     epilogue warpgroup with setmaxnreg.
 //
+// PAIR = 2 (a cluster of two CTAs on the two SMs of a TPC, 256 x 256 tiles):
+// each CTA loads its own 128 rows of A and its own 128 columns of B, so the
+// shared-memory bytes written by TMA and read by the tensor core per SM are
+// half those of a one-SM 128 x 256 tile for the same MMA work.  The even CTA
+// (rank 0) owns the ring's full barriers and the accumulator's empty
+// barriers: both CTAs' TMA loads complete on the even CTA's full[s] (the even
+// CTA alone registers the pair's bytes with expect_tx), the even CTA's lane
+// issues the M = 256 MMAs, and its commits multicast to empty[s] and
+// acc_full[a] of both CTAs; the epilogue warps of both CTAs arrive on the even
+// CTA's acc_empty[a] (8 arrivals).  Each CTA drains its own 128 rows of the
+// accumulator from its own TMEM.
+//
 // Shared-memory ring stage (both kinds: 128 bytes of K per row):
 //   A: 128 rows (M) x 128 B, K-major, TMA 128-byte swizzle      16 KiB
-//   B: BK rows (K) x 256 columns (N), N-major (B is row-major [K, N]),
-//      stored as 256*esize/128 panels of BK rows x 128 B          32 KiB
-// kind     BK  MMA K  panels  panel bytes
-// bf16     64   16      4       8 KiB
-// tf32     32    8      8       4 KiB
+//   B: 256 / PAIR columns of this CTA:
+//      bf16: N-major panels of 64 rows (K) x 128 B (64 columns)  8 KiB each
+//      tf32: K-major, one 128-byte row of K per column
+//   PAIR = 1: 48 KiB per stage, PAIR = 2: 32 KiB per stage.
+// kind     BK  MMA K
+// bf16     64   16
+// tf32     32    8
 #include "gbr_internal.h"
 
 #include <cuda_bf16.h>
@@ -54,30 +69,38 @@ template <int KIND>
 struct Kind;
 template <>
 struct Kind<kUmmaBf16> {
-    static constexpr uint32_t esize = 2, bk = 64, mma_k = 16, panel_cols = 64, panels = 4;
+    static constexpr uint32_t esize = 2, bk = 64, mma_k = 16, panel_cols = 64;
     static constexpr uint32_t ab_format = 1;          // BF16
     static constexpr uint32_t out_chunk_cols = 64;    // 64 bf16 = 128 B per row
     static constexpr bool b_kmajor = false;           // B stays row-major [K, N]
 };
 template <>
 struct Kind<kUmmaTf32> {
-    static constexpr uint32_t esize = 4, bk = 32, mma_k = 8, panel_cols = 32, panels = 8;
+    static constexpr uint32_t esize = 4, bk = 32, mma_k = 8, panel_cols = 32;
     static constexpr uint32_t ab_format = 2;          // TF32
     static constexpr uint32_t out_chunk_cols = 32;    // 32 fp32 = 128 B per row
     static constexpr bool b_kmajor = true;            // B arrives transposed, Bt[N, K]
 };
 
+template <int PAIR>
+struct Pair {
+    static constexpr uint32_t tile_m = 128 * PAIR;           // rows per output tile
+    static constexpr uint32_t b_cols = kUmmaBN / PAIR;       // B columns held per CTA
+    static constexpr uint32_t b_bytes = b_cols * 128;        // B bytes per CTA per stage
+    static constexpr uint32_t stage_bytes = kUmmaAStageBytes + b_bytes;
+};
+
 // Instruction descriptor, kind::f16 / kind::tf32: fp32 accumulator, A K-major,
-// B MN-major (bf16) or K-major (tf32), M = 128, N = 256, dense, no negation.
-template <int KIND>
+// B MN-major (bf16) or K-major (tf32), M = 128 * PAIR, N = 256, dense.
+template <int KIND, int PAIR>
 __host__ __device__ constexpr uint32_t make_idesc() {
-    return (1u << 4)                              // D format: f32
-           | (Kind<KIND>::ab_format << 7)         // A format
-           | (Kind<KIND>::ab_format << 10)        // B format
-           | (0u << 15)                           // A: K-major
-           | ((Kind<KIND>::b_kmajor ? 0u : 1u) << 16)  // B: K-major / MN-major
-           | ((uint32_t(kUmmaBN) >> 3) << 17)     // N / 8
-           | ((uint32_t(kUmmaBM) >> 4) << 24);    // M / 16
+    return (1u << 4)                                     // D format: f32
+           | (Kind<KIND>::ab_format << 7)                // A format
+           | (Kind<KIND>::ab_format << 10)               // B format
+           | (0u << 15)                                  // A: K-major
+           | ((Kind<KIND>::b_kmajor ? 0u : 1u) << 16)    // B: K-major / MN-major
+           | ((uint32_t(kUmmaBN) >> 3) << 17)            // N / 8
+           | ((Pair<PAIR>::tile_m >> 4) << 24);          // M / 16
 }
 
 // Shared-memory matrix descriptor with 128-byte swizzling.
@@ -106,27 +129,28 @@ struct UmmaParams {
 };
 
 struct TileInfo {
-    int32_t a_row;   // row coordinate of the A/X box
-    int32_t c_row;   // row coordinate of the C box in mapC[group]
-    int32_t n0;      // first output column
+    int32_t a_row;   // row coordinate of this CTA's A/X box
+    int32_t c_row;   // row coordinate of this CTA's C rows in mapC[group]
+    int32_t n0;      // first output column of the tile
     int32_t group;
 };
 
-template <bool GROUPED>
-__device__ __forceinline__ TileInfo decode_tile(const UmmaParams<GROUPED>& P, uint32_t t) {
+template <bool GROUPED, int PAIR>
+__device__ __forceinline__ TileInfo decode_tile(const UmmaParams<GROUPED>& P, uint32_t t,
+                                                uint32_t rank) {
     TileInfo ti;
     uint32_t mt, nt;
     if (!GROUPED) {
         raster_tile(t, P.s.m_tiles, P.s.n_tiles, P.s.group_m, mt, nt);
-        ti.a_row = int32_t(mt) * kUmmaBM;
-        ti.c_row = ti.a_row;
+        ti.c_row = int32_t(mt * Pair<PAIR>::tile_m + rank * 128);
+        ti.a_row = ti.c_row;
         ti.group = 0;
     } else {
         int e = 0;
         while (e + 1 < P.g.num_groups && int32_t(t) >= P.g.tile_start[e + 1]) ++e;
         raster_tile(t - uint32_t(P.g.tile_start[e]), uint32_t(P.g.m_tiles[e]), P.s.n_tiles,
                     P.s.group_m, mt, nt);
-        ti.c_row = int32_t(mt) * kUmmaBM;
+        ti.c_row = int32_t(mt * Pair<PAIR>::tile_m + rank * 128);
         ti.a_row = P.g.row_off[e] + ti.c_row;
         ti.group = e;
     }
@@ -134,19 +158,21 @@ __device__ __forceinline__ TileInfo decode_tile(const UmmaParams<GROUPED>& P, ui
     return ti;
 }
 
-template <int KIND, bool GROUPED>
+template <int KIND, bool GROUPED, int PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_umma_kernel(const __grid_constant__ UmmaParams<GROUPED> P) {
     using K_ = Kind<KIND>;
+    using PR = Pair<PAIR>;
+    constexpr bool kCl = PAIR == 2;                      // cluster-scope waits
     constexpr uint32_t kPanelBytes = K_::bk * 128;
-    constexpr uint32_t kIdesc = make_idesc<KIND>();
+    constexpr uint32_t kIdesc = make_idesc<KIND, PAIR>();
     constexpr uint32_t kChunks = kUmmaBN / K_::out_chunk_cols;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = align_1024(smem_raw);
     const int S = P.s.stages;
     uint8_t* ring = base;
-    uint8_t* epi = ring + size_t(S) * kUmmaStageBytes;
+    uint8_t* epi = ring + size_t(S) * PR::stage_bytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(epi + kUmmaEpiBytes);
     uint64_t* empty = full + S;
     uint64_t* acc_full = empty + S;
@@ -156,6 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t rank = PAIR == 2 ? ptx::cluster_ctarank() : 0u;
+    const uint32_t unit = blockIdx.x / PAIR, units = gridDim.x / PAIR;
     const GemmShape& s = P.s;
 
     if (threadIdx.x == 0) {
@@ -164,8 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(ptx::smem_addr(empty + i), 1);   // one tcgen05.commit
         }
         for (int a = 0; a < 2; ++a) {
-            ptx::mbar_init(ptx::smem_addr(acc_full + a), 1);   // one tcgen05.commit
-            ptx::mbar_init(ptx::smem_addr(acc_empty + a), 4);  // one arrive per epilogue warp
+            ptx::mbar_init(ptx::smem_addr(acc_full + a), 1);                // one commit
+            ptx::mbar_init(ptx::smem_addr(acc_empty + a), 4 * PAIR);        // epilogue warps
         }
         ptx::mbar_init(ptx::smem_addr(drain), 1);
         *abort_flag = 0;
@@ -175,11 +203,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&P.mapB);
     }
     if (warp == 2) {
-        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), kTmemCols);
-        ptx::tmem_relinquish_alloc_permit();
+        if (PAIR == 2) {
+            ptx::tmem_alloc_pair(ptx::smem_addr(tmem_holder), kTmemCols);
+            ptx::tmem_relinquish_alloc_permit_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_addr(tmem_holder), kTmemCols);
+            ptx::tmem_relinquish_alloc_permit();
+        }
     }
     ptx::tc_fence_before_sync();
-    __syncthreads();
+    if (PAIR == 2)
+        ptx::cluster_sync_all();   // barriers of both CTAs initialised before any remote use
+    else
+        __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
 
@@ -190,63 +226,78 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ring_base = ptx::smem_addr(ring);
             uint32_t it = 0;
             bool ok = true;
-            for (uint32_t t = blockIdx.x; ok && t < uint32_t(s.num_tiles); t += gridDim.x) {
-                const TileInfo ti = decode_tile<GROUPED>(P, t);
+            for (uint32_t t = unit; ok && t < uint32_t(s.num_tiles); t += units) {
+                const TileInfo ti = decode_tile<GROUPED, PAIR>(P, t, rank);
+                const int32_t bcol0 = ti.n0 + int32_t(rank * PR::b_cols);
                 for (int kb = 0; kb < s.num_kb; ++kb, ++it) {
                     const uint32_t slot = it % S, ph = (it / S) & 1u;
-                    if (!mbar_wait(ptx::smem_addr(empty + slot), ph ^ 1u, s.ctl, abort_flag,
-                                   kSiteProducerEmpty, it)) {
+                    if (!mbar_wait<kCl>(ptx::smem_addr(empty + slot), ph ^ 1u, s.ctl, abort_flag,
+                                        kSiteProducerEmpty, it)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = ptx::smem_addr(full + slot);
-                    ptx::mbar_arrive_expect_tx(fb, kUmmaStageBytes);
-                    const uint32_t a_dst = ring_base + slot * kUmmaStageBytes;
+                    const uint32_t fb_local = ptx::smem_addr(full + slot);
+                    const uint32_t fb = PAIR == 2 ? ptx::mapa_shared(fb_local, 0) : fb_local;
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, PAIR * PR::stage_bytes);
+                    const uint32_t a_dst = ring_base + slot * PR::stage_bytes;
                     const uint32_t b_dst = a_dst + kUmmaAStageBytes;
                     const int32_t k0 = kb * int32_t(K_::bk);
-                    ptx::tma_load_2d(a_dst, &P.mapA, fb, k0, ti.a_row);
+                    if (PAIR == 2)
+                        ptx::tma_load_2d_pair(a_dst, &P.mapA, fb, k0, ti.a_row);
+                    else
+                        ptx::tma_load_2d(a_dst, &P.mapA, fb, k0, ti.a_row);
                     if (K_::b_kmajor) {
-                        // Bt[N, K]: one 256-row box, 128 bytes of K per row.
-                        ptx::tma_load_2d(b_dst, &P.mapB, fb, k0, ti.n0);
+                        // Bt[N, K]: one box of this CTA's b_cols rows, 128 bytes of K each.
+                        if (PAIR == 2)
+                            ptx::tma_load_2d_pair(b_dst, &P.mapB, fb, k0, bcol0);
+                        else
+                            ptx::tma_load_2d(b_dst, &P.mapB, fb, k0, bcol0);
                     } else {
 #pragma unroll
-                        for (uint32_t j = 0; j < K_::panels; ++j) {
-                            const int32_t n = ti.n0 + int32_t(j * K_::panel_cols);
-                            if (GROUPED)
-                                ptx::tma_load_3d(b_dst + j * kPanelBytes, &P.mapB, fb, n, k0,
-                                                 ti.group);
-                            else
-                                ptx::tma_load_2d(b_dst + j * kPanelBytes, &P.mapB, fb, n, k0);
+                        for (uint32_t j = 0; j < PR::b_cols / K_::panel_cols; ++j) {
+                            const int32_t n = bcol0 + int32_t(j * K_::panel_cols);
+                            const uint32_t d = b_dst + j * kPanelBytes;
+                            if (GROUPED) {
+                                if (PAIR == 2)
+                                    ptx::tma_load_3d_pair(d, &P.mapB, fb, n, k0, ti.group);
+                                else
+                                    ptx::tma_load_3d(d, &P.mapB, fb, n, k0, ti.group);
+                            } else {
+                                if (PAIR == 2)
+                                    ptx::tma_load_2d_pair(d, &P.mapB, fb, n, k0);
+                                else
+                                    ptx::tma_load_2d(d, &P.mapB, fb, n, k0);
+                            }
                         }
                     }
                 }
             }
-            if (*abort_flag) {
+            if (*abort_flag && rank == 0) {
                 const uint32_t n = it < uint32_t(S) ? it : uint32_t(S);
                 for (uint32_t j = it - n; j < it; ++j)
                     mbar_wait_drain(ptx::smem_addr(full + j % S), (j / S) & 1u, s.ctl.timeout_ns);
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1 && lane == 0 && rank == 0) {
             // ---------------------------------------------------- MMA issuer
             const uint32_t ring_base = ptx::smem_addr(ring);
             uint32_t it = 0, tl = 0;
             bool ok = true;
-            for (uint32_t t = blockIdx.x; ok && t < uint32_t(s.num_tiles); t += gridDim.x, ++tl) {
+            for (uint32_t t = unit; ok && t < uint32_t(s.num_tiles); t += units, ++tl) {
                 const uint32_t a = tl & 1u, aph = (tl >> 1) & 1u;
-                if (!mbar_wait(ptx::smem_addr(acc_empty + a), aph ^ 1u, s.ctl, abort_flag,
-                               kSiteMmaAccEmpty, tl))
+                if (!mbar_wait<kCl>(ptx::smem_addr(acc_empty + a), aph ^ 1u, s.ctl, abort_flag,
+                                    kSiteMmaAccEmpty, tl))
                     break;
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + a * kAccCols;
                 for (int kb = 0; kb < s.num_kb; ++kb, ++it) {
                     const uint32_t slot = it % S, ph = (it / S) & 1u;
-                    if (!mbar_wait(ptx::smem_addr(full + slot), ph, s.ctl, abort_flag,
-                                   kSiteMmaFull, it)) {
+                    if (!mbar_wait<kCl>(ptx::smem_addr(full + slot), ph, s.ctl, abort_flag,
+                                        kSiteMmaFull, it)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    const uint32_t a_base = ring_base + slot * kUmmaStageBytes;
+                    const uint32_t a_base = ring_base + slot * PR::stage_bytes;
                     const uint32_t b_base = a_base + kUmmaAStageBytes;
 #pragma unroll
                     for (uint32_t k = 0; k < 128 / (K_::mma_k * K_::esize); ++k) {
@@ -255,21 +306,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                             K_::b_kmajor
                                 ? sw128_desc(b_base + k * K_::mma_k * K_::esize, 16, 1024)
                                 : sw128_desc(b_base + k * K_::mma_k * 128, kPanelBytes, 1024);
-                        if (KIND == kUmmaBf16)
-                            ptx::mma_f16(d_tmem, ad, bd, kIdesc, (kb | k) != 0);
-                        else
-                            ptx::mma_tf32(d_tmem, ad, bd, kIdesc, (kb | k) != 0);
+                        const uint32_t acc = (kb | k) != 0;
+                        if (PAIR == 2) {
+                            if (KIND == kUmmaBf16)
+                                ptx::mma_f16_pair(d_tmem, ad, bd, kIdesc, acc);
+                            else
+                                ptx::mma_tf32_pair(d_tmem, ad, bd, kIdesc, acc);
+                        } else {
+                            if (KIND == kUmmaBf16)
+                                ptx::mma_f16(d_tmem, ad, bd, kIdesc, acc);
+                            else
+                                ptx::mma_tf32(d_tmem, ad, bd, kIdesc, acc);
+                        }
                     }
-                    ptx::mma_commit(ptx::smem_addr(empty + slot));
+                    if (PAIR == 2)
+                        ptx::mma_commit_pair_multicast(ptx::smem_addr(empty + slot), 0x3);
+                    else
+                        ptx::mma_commit(ptx::smem_addr(empty + slot));
                 }
                 if (!ok) break;
-                if (s.num_kb > 0)
-                    ptx::mma_commit(ptx::smem_addr(acc_full + a));
-                else
-                    ptx::mbar_arrive(ptx::smem_addr(acc_full + a));
+                if (s.num_kb > 0) {
+                    if (PAIR == 2)
+                        ptx::mma_commit_pair_multicast(ptx::smem_addr(acc_full + a), 0x3);
+                    else
+                        ptx::mma_commit(ptx::smem_addr(acc_full + a));
+                } else {
+                    const uint32_t af = ptx::smem_addr(acc_full + a);
+                    if (PAIR == 2) {
+                        ptx::mbar_arrive_cluster(ptx::mapa_shared(af, 0));
+                        ptx::mbar_arrive_cluster(ptx::mapa_shared(af, 1));
+                    } else {
+                        ptx::mbar_arrive(af);
+                    }
+                }
             }
-            // No MMA may still be running when TMEM is released.
-            ptx::mma_commit(ptx::smem_addr(drain));
+            // No MMA may still be running when TMEM (or the peer's smem) is released.
+            if (PAIR == 2)
+                ptx::mma_commit_pair_multicast(ptx::smem_addr(drain), 0x1);
+            else
+                ptx::mma_commit(ptx::smem_addr(drain));
             mbar_wait_drain(ptx::smem_addr(drain), 0, s.ctl.timeout_ns);
         }
     } else {
@@ -282,11 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t swz = lane & 7u;
         const bool zero_acc = s.num_kb == 0;
         uint32_t tl = 0, chunk_ctr = 0;
-        for (uint32_t t = blockIdx.x; t < uint32_t(s.num_tiles); t += gridDim.x, ++tl) {
-            const TileInfo ti = decode_tile<GROUPED>(P, t);
+        for (uint32_t t = unit; t < uint32_t(s.num_tiles); t += units, ++tl) {
+            const TileInfo ti = decode_tile<GROUPED, PAIR>(P, t, rank);
             const uint32_t a = tl & 1u, aph = (tl >> 1) & 1u;
-            if (!mbar_wait_warp(ptx::smem_addr(acc_full + a), aph, s.ctl, abort_flag,
-                                kSiteEpiAccFull, tl))
+            if (!mbar_wait_warp<kCl>(ptx::smem_addr(acc_full + a), aph, s.ctl, abort_flag,
+                                     kSiteEpiAccFull, tl))
                 break;
             ptx::tc_fence_after_sync();
             const float* bias = s.bias + (GROUPED ? P.bias_group_stride * ti.group : 0);
@@ -303,7 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (c + 1 == kChunks) {
                         ptx::tc_fence_before_sync();
                         __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(acc_empty + a));
+                        if (lane == 0) {
+                            const uint32_t ae = ptx::smem_addr(acc_empty + a);
+                            if (PAIR == 2)
+                                ptx::mbar_arrive_cluster(ptx::mapa_shared(ae, 0));
+                            else
+                                ptx::mbar_arrive(ae);
+                        }
                     }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -332,7 +413,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (c + 1 == kChunks) {
                         ptx::tc_fence_before_sync();
                         __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(acc_empty + a));
+                        if (lane == 0) {
+                            const uint32_t ae = ptx::smem_addr(acc_empty + a);
+                            if (PAIR == 2)
+                                ptx::mbar_arrive_cluster(ptx::mapa_shared(ae, 0));
+                            else
+                                ptx::mbar_arrive(ae);
+                        }
                     }
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
@@ -370,48 +457,92 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     __syncwarp();
     ptx::tc_fence_before_sync();
-    __syncthreads();
+    if (PAIR == 2)
+        ptx::cluster_sync_all();   // no CTA leaves while its peer may still touch its smem
+    else
+        __syncthreads();
     if (warp == 2) {
         ptx::tc_fence_after_sync();
-        ptx::tmem_dealloc(tmem_base, kTmemCols);
+        if (PAIR == 2)
+            ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            ptx::tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
-template <int KIND, bool GROUPED>
+template <int KIND, bool GROUPED, int PAIR>
 void* kernel_ptr() {
-    return reinterpret_cast<void*>(&gemm_umma_kernel<KIND, GROUPED>);
+    return reinterpret_cast<void*>(&gemm_umma_kernel<KIND, GROUPED, PAIR>);
 }
 
-void* select_kernel(int kind, bool grouped) {
-    if (kind == kUmmaBf16) return grouped ? kernel_ptr<kUmmaBf16, true>() : kernel_ptr<kUmmaBf16, false>();
-    return grouped ? kernel_ptr<kUmmaTf32, true>() : kernel_ptr<kUmmaTf32, false>();
+void* select_kernel(int kind, bool grouped, int pair) {
+    if (pair == 2) {
+        if (kind == kUmmaBf16)
+            return grouped ? kernel_ptr<kUmmaBf16, true, 2>() : kernel_ptr<kUmmaBf16, false, 2>();
+        return grouped ? kernel_ptr<kUmmaTf32, true, 2>() : kernel_ptr<kUmmaTf32, false, 2>();
+    }
+    if (kind == kUmmaBf16)
+        return grouped ? kernel_ptr<kUmmaBf16, true, 1>() : kernel_ptr<kUmmaBf16, false, 1>();
+    return grouped ? kernel_ptr<kUmmaTf32, true, 1>() : kernel_ptr<kUmmaTf32, false, 1>();
+}
+
+template <bool GROUPED>
+cudaError_t launch_pair(int kind, const UmmaParams<GROUPED>& P, int grid, size_t smem,
+                        cudaStream_t stream) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {const_cast<UmmaParams<GROUPED>*>(&P)};
+    return cudaLaunchKernelExC(&cfg, select_kernel(kind, GROUPED, 2), args);
 }
 
 }  // namespace
 
-size_t umma_smem_bytes(int stages) {
-    const size_t need = 1024 + size_t(stages) * kUmmaStageBytes + kUmmaEpiBytes + 256;
+size_t umma_ring_bytes(int stages, int pair) {
+    const size_t stage = pair == 2 ? Pair<2>::stage_bytes : Pair<1>::stage_bytes;
+    return 1024 + size_t(stages) * stage + kUmmaEpiBytes + 256;
+}
+
+size_t umma_smem_bytes(int stages, int pair) {
+    const size_t need = umma_ring_bytes(stages, pair);
     // At least half the SM's shared memory, so that two CTAs never share an
     // SM and compete for its 512 TMEM columns.
     const size_t floor_one_cta = 120 * 1024;
     return need > floor_one_cta ? need : floor_one_cta;
 }
+size_t umma_smem_bytes(int stages) { return umma_smem_bytes(stages, 1); }
 
-cudaError_t umma_prepare(int kind, bool grouped, size_t smem) {
-    return cudaFuncSetAttribute(select_kernel(kind, grouped),
+cudaError_t umma_prepare(int kind, bool grouped, int pair, size_t smem) {
+    return cudaFuncSetAttribute(select_kernel(kind, grouped, pair),
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
 }
+cudaError_t umma_prepare(int kind, bool grouped, size_t smem) {
+    return umma_prepare(kind, grouped, 1, smem);
+}
 
-cudaError_t umma_check_registers(int kind, bool grouped, int* regs) {
+cudaError_t umma_check_registers(int kind, bool grouped, int pair, int* regs) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, select_kernel(kind, grouped));
+    cudaError_t e = cudaFuncGetAttributes(&fa, select_kernel(kind, grouped, pair));
     if (e != cudaSuccess) return e;
     *regs = fa.numRegs;
     const long need = 128L * kRegsWG0 + 128L * kRegsWG1;
     return (long(fa.numRegs) * kThreads >= need) ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
+cudaError_t umma_check_registers(int kind, bool grouped, int* regs) {
+    return umma_check_registers(kind, grouped, 1, regs);
+}
 
-cudaError_t launch_gemm_umma(int kind, const CUtensorMap& mapA, const CUtensorMap& mapB,
+cudaError_t launch_gemm_umma(int kind, int pair, const CUtensorMap& mapA, const CUtensorMap& mapB,
                              const CUtensorMap& mapC, const GemmShape& s, int grid, size_t smem,
                              cudaStream_t stream) {
     UmmaParams<false> P;
@@ -421,14 +552,20 @@ cudaError_t launch_gemm_umma(int kind, const CUtensorMap& mapA, const CUtensorMa
     P.mapC[0] = mapC;
     P.s = s;
     P.bias_group_stride = 0;
+    if (pair == 2) return launch_pair<false>(kind, P, grid, smem, stream);
     if (kind == kUmmaBf16)
-        gemm_umma_kernel<kUmmaBf16, false><<<grid, kThreads, smem, stream>>>(P);
+        gemm_umma_kernel<kUmmaBf16, false, 1><<<grid, kThreads, smem, stream>>>(P);
     else
-        gemm_umma_kernel<kUmmaTf32, false><<<grid, kThreads, smem, stream>>>(P);
+        gemm_umma_kernel<kUmmaTf32, false, 1><<<grid, kThreads, smem, stream>>>(P);
     return cudaGetLastError();
 }
+cudaError_t launch_gemm_umma(int kind, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                             const CUtensorMap& mapC, const GemmShape& s, int grid, size_t smem,
+                             cudaStream_t stream) {
+    return launch_gemm_umma(kind, 1, mapA, mapB, mapC, s, grid, smem, stream);
+}
 
-cudaError_t launch_gemm_umma_grouped(const CUtensorMap& mapX, const CUtensorMap& mapW,
+cudaError_t launch_gemm_umma_grouped(int pair, const CUtensorMap& mapX, const CUtensorMap& mapW,
                                      const CUtensorMap* mapsC, const GroupTable& g,
                                      const GemmShape& s, int64_t bias_group_stride, int grid,
                                      size_t smem, cudaStream_t stream) {
@@ -440,7 +577,8 @@ cudaError_t launch_gemm_umma_grouped(const CUtensorMap& mapX, const CUtensorMap&
     P.s = s;
     P.g = g;
     P.bias_group_stride = bias_group_stride;
-    gemm_umma_kernel<kUmmaBf16, true><<<grid, kThreads, smem, stream>>>(P);
+    if (pair == 2) return launch_pair<true>(kUmmaBf16, P, grid, smem, stream);
+    gemm_umma_kernel<kUmmaBf16, true, 1><<<grid, kThreads, smem, stream>>>(P);
     return cudaGetLastError();
 }
 

@@ -52,3 +52,19 @@ def sample_points(M, N, n, seed, extra_rows=(), extra_cols=()):
         ms += list(rows)
         ns += [c] * len(rows)
     return np.array(ms, dtype=np.int64), np.array(ns, dtype=np.int64)
+
+
+class tuned:
+    """Forces the tensor-core GEMM variant (1: one CTA per tile, 2: CTA pair)
+    for the duration of a with-block, then restores the automatic choice."""
+
+    def __init__(self, gbr, pair):
+        self.gbr, self.pair = gbr, pair
+
+    def __enter__(self):
+        self.gbr.gemm_tuning(self.pair, -1)
+        return self
+
+    def __exit__(self, *exc):
+        self.gbr.gemm_tuning(-1, -1)
+        return False

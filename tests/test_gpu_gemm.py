@@ -11,7 +11,7 @@ import torch
 import oracle
 from mbarrier_gemm_pipelines_gb300 import inputs
 from gpu_helpers import (TOL, load_library, rel_frobenius, require_gpu, sample_points,
-                         to_host_f64)
+                         to_host_f64, tuned)
 
 pytestmark = pytest.mark.gpu
 
@@ -52,36 +52,72 @@ SHAPES = [(128, 128, 32), (256, 512, 256), (200, 136, 104), (129, 264, 40), (1, 
           (300, 520, 200), (640, 384, 1000), (383, 776, 1352)]
 
 
-@pytest.mark.parametrize("dtype", ["ffma", "tf32", "bf16"])
+VARIANTS = [("ffma", -1), ("tf32", 1), ("tf32", 2), ("bf16", 1), ("bf16", 2)]
+
+
+@pytest.mark.parametrize("dtype,pair", VARIANTS)
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_small_shapes(gbr, dtype, M, N, K):
+def test_small_shapes(gbr, dtype, pair, M, N, K):
     A, B, bias = inputs.gemm_uniform(M, N, K, seed=M * 31 + N * 7 + K)
     if dtype == "bf16":
         A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
-    got = _run(gbr, A, B, bias, dtype, 2)
+    with tuned(gbr, pair):
+        got = _run(gbr, A, B, bias, dtype, 2)
     _check_full(got, A.float(), B.float(), bias, dtype)
 
 
-@pytest.mark.parametrize("dtype", ["ffma", "tf32", "bf16"])
-def test_stage_sweep(gbr, dtype):
+@pytest.mark.parametrize("dtype,pair", VARIANTS)
+def test_stage_sweep(gbr, dtype, pair):
     M, N, K = 384, 512, 640
     A, B, bias = inputs.gemm_normal(M, N, K, seed=5)
     if dtype == "bf16":
         A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
     smax = gbr.max_stages(gbr.OP_GEMM, {"ffma": 0, "tf32": 1, "bf16": 2}[dtype])
     assert smax >= 4
-    for S in range(1, smax + 1):
-        got = _run(gbr, A, B, bias, dtype, S)
-        _check_full(got, A.float(), B.float(), bias, dtype)
+    if pair == 1:
+        smax = 4                                   # one CTA per tile holds 4 stages
+    with tuned(gbr, pair):
+        for S in range(1, smax + 1):
+            got = _run(gbr, A, B, bias, dtype, S)
+            _check_full(got, A.float(), B.float(), bias, dtype)
 
 
-@pytest.mark.parametrize("dtype", ["ffma", "tf32", "bf16"])
-def test_k_zero_is_relu_bias(gbr, dtype):
+@pytest.mark.parametrize("dtype", ["tf32", "bf16"])
+def test_pair_and_single_agree(gbr, dtype):
+    """The CTA-pair kernel (M = 256 MMAs) and the one-CTA kernel add the same
+    products in the same K order, so their outputs agree to the output rounding."""
+    A, B, bias = inputs.gemm_normal(520, 776, 1352, seed=6)
+    if dtype == "bf16":
+        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    outs = []
+    for pair in (1, 2):
+        with tuned(gbr, pair):
+            outs.append(_run(gbr, A, B, bias, dtype, 3))
+    assert rel_frobenius(outs[1], outs[0]) <= TOL[dtype] / 10
+    _check_full(outs[1], A.float(), B.float(), bias, dtype)
+
+
+def test_forced_single_rejects_deep_ring(gbr):
+    A = torch.zeros((256, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((64, 256), dtype=torch.bfloat16, device="cuda")
+    bias = torch.zeros(256, device="cuda")
+    with tuned(gbr, 1):
+        with pytest.raises(gbr.GbrError) as e:
+            gbr.gemm_bias_relu(A, B, bias, dtype="bf16", stages=5)
+    assert e.value.code == 4
+    C = gbr.gemm_bias_relu(A, B, bias, dtype="bf16", stages=6)   # auto: the pair kernel
+    gbr.check_device()
+    assert bool((C == 0).all())
+
+
+@pytest.mark.parametrize("dtype,pair", VARIANTS)
+def test_k_zero_is_relu_bias(gbr, dtype, pair):
     bias = torch.linspace(-2, 2, 264)
     t = torch.bfloat16 if dtype == "bf16" else torch.float32
-    A = torch.empty((70, 0), dtype=t)
+    A = torch.empty((270, 0), dtype=t)
     B = torch.empty((0, 264), dtype=t)
-    C = gbr.gemm_bias_relu(A.cuda(), B.cuda(), bias.cuda(), dtype=dtype, stages=2)
+    with tuned(gbr, pair):
+        C = gbr.gemm_bias_relu(A.cuda(), B.cuda(), bias.cuda(), dtype=dtype, stages=2)
     gbr.check_device()
     expect = oracle.gemm_bias_relu(A.float(), B.float(), bias)
     if dtype == "bf16":
@@ -163,16 +199,20 @@ def _sampled(gbr, A, B, bias, dtype, stages, npts, seed):
     return C
 
 
-@pytest.mark.parametrize("dtype,S", [("ffma", 3), ("ffma", 4), ("tf32", 3), ("tf32", 4)])
-def test_config3_fp32_4096(gbr, dtype, S):
+@pytest.mark.parametrize("dtype,S,pair", [("ffma", 3, -1), ("ffma", 4, -1), ("tf32", 3, -1),
+                                           ("tf32", 4, -1), ("tf32", 4, 1)])
+def test_config3_fp32_4096(gbr, dtype, S, pair):
     A, B, bias = inputs.workload("gemm_fp32")
-    _sampled(gbr, A, B, bias, dtype, S, 3000, seed=2)
+    with tuned(gbr, pair):
+        _sampled(gbr, A, B, bias, dtype, S, 3000, seed=2)
 
 
-@pytest.mark.parametrize("S", [4])
-def test_config4_bf16_8192(gbr, S):
+@pytest.mark.parametrize("S,pair", [(4, -1), (5, -1), (6, -1), (4, 1)])
+def test_config4_bf16_8192(gbr, S, pair):
+    """bf16 8192^3, 4-6 stage ring (the pair kernel by default; one CTA per tile at S=4)."""
     A, B, bias = inputs.workload("gemm_bf16")
-    C = _sampled(gbr, A, B, bias, "bf16", S, 3000, seed=3)
+    with tuned(gbr, pair):
+        C = _sampled(gbr, A, B, bias, "bf16", S, 3000, seed=3)
     assert bool((C >= 0).all())
 
 

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from mbarrier_gemm_pipelines_gb300 import inputs
-from gpu_helpers import TOL, load_library, rel_frobenius, require_gpu, to_host_f64
+from gpu_helpers import TOL, load_library, rel_frobenius, require_gpu, to_host_f64, tuned
 
 pytestmark = pytest.mark.gpu
 
@@ -23,11 +23,13 @@ def gbr():
     ([300, 300, 300], 128, 264),
     ([0, 0, 129], 72, 512),
 ])
-def test_grouped_small(gbr, counts, K, N):
+@pytest.mark.parametrize("pair", [1, 2])
+def test_grouped_small(gbr, counts, K, N, pair):
     G = len(counts)
     cnt, X, W, b = inputs.grouped(tokens=sum(counts), experts=G, K=K, N=N, seed=sum(counts) + K)
     cnt = counts                                          # fixed counts for the edge cases
-    C = gbr.gemm_bias_relu_grouped(X.cuda(), W.cuda(), b.cuda(), cnt, stages=3)
+    with tuned(gbr, pair):
+        C = gbr.gemm_bias_relu_grouped(X.cuda(), W.cuda(), b.cuda(), cnt, stages=3)
     gbr.check_device()
     ref = oracle.gemm_bias_relu_grouped(X.float(), W.float(), b, cnt)
     got = to_host_f64(C)
@@ -35,18 +37,20 @@ def test_grouped_small(gbr, counts, K, N):
     assert np.abs(got - ref).max() <= 0.2 * np.abs(ref).max()
 
 
-def test_grouped_matches_dense_per_expert(gbr):
+@pytest.mark.parametrize("pair", [1, 2])
+def test_grouped_matches_dense_per_expert(gbr, pair):
     """Each expert's rows equal the dense kernel run on that expert alone."""
     counts = [200, 77, 300]
     cnt, X, W, b = inputs.grouped(tokens=sum(counts), experts=3, K=256, N=512, seed=11)
     dX, dW, db = X.cuda(), W.cuda(), b.cuda()
-    C = gbr.gemm_bias_relu_grouped(dX, dW, db, counts, stages=4)
-    off = 0
-    for e, n_e in enumerate(counts):
-        Ce = gbr.gemm_bias_relu(dX[off:off + n_e].contiguous(), dW[e].contiguous(),
-                                db[e].contiguous(), dtype="bf16", stages=4)
-        assert torch.equal(C[off:off + n_e], Ce)
-        off += n_e
+    with tuned(gbr, pair):
+        C = gbr.gemm_bias_relu_grouped(dX, dW, db, counts, stages=4)
+        off = 0
+        for e, n_e in enumerate(counts):
+            Ce = gbr.gemm_bias_relu(dX[off:off + n_e].contiguous(), dW[e].contiguous(),
+                                    db[e].contiguous(), dtype="bf16", stages=4)
+            assert torch.equal(C[off:off + n_e], Ce)
+            off += n_e
     gbr.check_device()
 
 
@@ -68,11 +72,13 @@ def test_grouped_rejects(gbr):
                                             bnd.BF16, 2, None) == bnd.ERR_INVALID
 
 
-def test_config5_moe_sampled(gbr):
+@pytest.mark.parametrize("pair,S", [(-1, 4), (1, 4), (2, 6)])
+def test_config5_moe_sampled(gbr, pair, S):
     """4096 tokens over 8 experts (Multinomial counts, seed 4), K = 4096,
     N = 14336, one launch; sampled positions in every expert."""
     counts, X, W, b = inputs.workload("grouped_bf16")
-    C = gbr.gemm_bias_relu_grouped(X.cuda(), W.cuda(), b.cuda(), counts, stages=4)
+    with tuned(gbr, pair):
+        C = gbr.gemm_bias_relu_grouped(X.cuda(), W.cuda(), b.cuda(), counts, stages=S)
     gbr.check_device()
     T, N = C.shape
     rng = np.random.default_rng(4)
