@@ -175,8 +175,13 @@ int gbr_copy_tuning(int store_lag, int ctas_per_sm);
  * cta_group::2 MMA, S <= 6).  Auto picks 2 when there is more than one
  * 128-row tile or S > 4 (grouped: when 256-row tiles waste at most ~10% more
  * rows).  group_m: -1 auto, else output-tile rows per raster band.
+ * l2_hint: L2 eviction priority of the A/B tile loads: -1 auto (none), 0 none,
+ * 1 both evict_last, 2 A evict_first + B evict_last, 3 A evict_last + B
+ * evict_first, 4 both evict_normal.  k_per_stage: -1 auto (1), 1 or 2 slices
+ * of 128 bytes of K per ring stage; with 2 a stage is twice as large (so the
+ * largest `stages` halves) and each full/empty handshake covers twice the MMAs.
  */
-int gbr_gemm_tuning(int cta_pair, int group_m);
+int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage);
 
 /*
  * Failure-detection self test: launches one CTA that waits, with the given

@@ -34,7 +34,7 @@ SIGNATURES = {
     "gbr_sm_count": (_i32, []),
     "gbr_set_wait_timeout_ns": (_i32, [_u64]),
     "gbr_copy_tuning": (_i32, [_i32, _i32]),
-    "gbr_gemm_tuning": (_i32, [_i32, _i32]),
+    "gbr_gemm_tuning": (_i32, [_i32, _i32, _i32, _i32]),
     "gbr_selftest_wait_timeout": (_i32, [_u64, _vp]),
     "gemm_bias_relu_tf32_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
 }
@@ -200,9 +200,12 @@ def copy_tuning(store_lag: int = -1, ctas_per_sm: int = -1) -> None:
     check(lib().gbr_copy_tuning(int(store_lag), int(ctas_per_sm)))
 
 
-def gemm_tuning(cta_pair: int = -1, group_m: int = -1) -> None:
-    """Tensor-core GEMM variant: cta_pair -1 auto, 1 one CTA per tile, 2 CTA pair."""
-    check(lib().gbr_gemm_tuning(int(cta_pair), int(group_m)))
+def gemm_tuning(cta_pair: int = -1, group_m: int = -1, l2_hint: int = -1,
+                k_per_stage: int = -1) -> None:
+    """Tensor-core GEMM variant: cta_pair -1 auto, 1 one CTA per tile, 2 CTA pair;
+    group_m raster band height in tiles; l2_hint operand-load L2 policy;
+    k_per_stage 128-byte K slices per ring stage (see gbr.h)."""
+    check(lib().gbr_gemm_tuning(int(cta_pair), int(group_m), int(l2_hint), int(k_per_stage)))
 
 
 def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:

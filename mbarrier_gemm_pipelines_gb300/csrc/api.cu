@@ -25,6 +25,8 @@ int g_copy_store_lag = -1;
 int g_copy_ctas_per_sm = -1;
 int g_gemm_pair = -1;      // -1 auto, 1 one CTA per tile, 2 CTA pair per tile
 int g_gemm_group_m = -1;   // -1 auto: tile rows per raster band
+int g_gemm_l2_hint = -1;   // -1 auto (none): L2 policy of the operand loads
+int g_gemm_k_sub = -1;     // -1 auto (1): 128-byte K slices per ring stage
 
 constexpr int kMaxDevices = 64;
 
@@ -165,9 +167,17 @@ size_t ffma_bytes_fn(int s) { return ffma_smem_bytes(s); }
 // The padding that keeps one CTA per SM is not part of the ring budget.
 size_t umma1_bytes_fn(int s) { return umma_ring_bytes(s, 1); }
 size_t umma2_bytes_fn(int s) { return umma_ring_bytes(s, 2); }
+size_t umma1k2_bytes_fn(int s) { return umma_ring_bytes(s, 1, 2); }
+size_t umma2k2_bytes_fn(int s) { return umma_ring_bytes(s, 2, 2); }
 
-int umma_max_stages(int pair, int smem_optin) {
+int umma_max_stages(int pair, int smem_optin, int k_sub = 1) {
+    if (k_sub == 2) return max_stages_for(pair == 2 ? umma2k2_bytes_fn : umma1k2_bytes_fn, smem_optin);
     return max_stages_for(pair == 2 ? umma2_bytes_fn : umma1_bytes_fn, smem_optin);
+}
+
+int k_sub_now() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_gemm_k_sub == 2 ? 2 : 1;
 }
 
 // Largest ring depth for the dtype (tcgen05: that of the CTA-pair kernel).
@@ -185,7 +195,9 @@ int choose_pair(int64_t rows, int stages, int smem_optin, int* pair) {
         std::lock_guard<std::mutex> lk(g_mu);
         forced = g_gemm_pair;
     }
-    const int max1 = umma_max_stages(1, smem_optin);
+    const int ks = k_sub_now();
+    const int max1 = umma_max_stages(1, smem_optin, ks);
+    const int max2 = umma_max_stages(2, smem_optin, ks);
     if (forced == 1) {
         if (stages > max1)
             return fail(GBR_ERR_SMEM, "stages=%d exceeds %d for one CTA per tile", stages, max1);
@@ -195,6 +207,8 @@ int choose_pair(int64_t rows, int stages, int smem_optin, int* pair) {
     } else {
         *pair = (rows > 128 || stages > max1) ? 2 : 1;
     }
+    if (*pair == 2 && stages > max2)
+        return fail(GBR_ERR_SMEM, "stages=%d exceeds %d for this stage size", stages, max2);
     return GBR_OK;
 }
 
@@ -202,6 +216,11 @@ int group_m_for(int pair) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_gemm_group_m > 0) return g_gemm_group_m;
     return pair == 2 ? 8 : 16;
+}
+
+uint32_t l2_hint_now() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_gemm_l2_hint > 0 ? uint32_t(g_gemm_l2_hint) : 0u;
 }
 
 int copy_max_stages(uint32_t tile_bytes, int smem_optin) {
@@ -264,12 +283,17 @@ int gbr_copy_tuning(int store_lag, int ctas_per_sm) {
     return GBR_OK;
 }
 
-int gbr_gemm_tuning(int cta_pair, int group_m) {
-    if (!(cta_pair == -1 || cta_pair == 1 || cta_pair == 2) || group_m == 0 || group_m < -1)
-        return fail(GBR_ERR_INVALID, "gbr_gemm_tuning: cta_pair in {-1,1,2}, group_m -1 or >= 1");
+int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage) {
+    if (!(cta_pair == -1 || cta_pair == 1 || cta_pair == 2) || group_m == 0 || group_m < -1 ||
+        l2_hint < -1 || l2_hint > 4 || !(k_per_stage == -1 || k_per_stage == 1 || k_per_stage == 2))
+        return fail(GBR_ERR_INVALID,
+                    "gbr_gemm_tuning: cta_pair in {-1,1,2}, group_m -1 or >= 1, l2_hint -1..4, "
+                    "k_per_stage in {-1,1,2}");
     std::lock_guard<std::mutex> lk(g_mu);
     g_gemm_pair = cta_pair;
     g_gemm_group_m = group_m;
+    g_gemm_l2_hint = l2_hint;
+    g_gemm_k_sub = k_per_stage;
     return GBR_OK;
 }
 
@@ -487,17 +511,19 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
     const uint32_t panel_cols = uint32_t(128 / es);  // B panel width; also the C store box width
     int pair = 1;
     if ((r = choose_pair(M, stages, c->smem_optin, &pair)) != GBR_OK) return r;
+    s.k_sub = uint32_t(k_sub_now());
     s.m_tiles = int32_t(cdiv(M, int64_t(kUmmaBM) * pair));
     s.n_tiles = int32_t(cdiv(N, kUmmaBN));
-    s.num_kb = int32_t(cdiv(K, bk));
+    s.num_kb = int32_t(cdiv(K, int64_t(bk) * s.k_sub));
     s.num_tiles = s.m_tiles * s.n_tiles;
     s.group_m = group_m_for(pair);
+    s.l2_hint = l2_hint_now();
     CUtensorMap ma, mb, mc;
     if ((r = encode_2d(&mc, dt, C, uint64_t(N), uint64_t(M), uint64_t(N) * es, panel_cols, 32,
                        CU_TENSOR_MAP_SWIZZLE_128B, "C")) != GBR_OK)
         return r;
     if ((r = check_umma_regs(*c, kind, false, pair)) != GBR_OK) return r;
-    const size_t smem = umma_smem_bytes(stages, pair);
+    const size_t smem = umma_smem_bytes(stages, pair, int(s.k_sub));
     if ((e = umma_prepare(kind, false, pair, smem)) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(tcgen05 GEMM)");
     const int grid = pair * int(std::min<int64_t>(s.num_tiles, c->sm_count / pair));
@@ -585,7 +611,8 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
     s.C = C;
     s.ctl = make_ctl(*c);
     s.n_tiles = int32_t(cdiv(N, kUmmaBN));
-    s.num_kb = int32_t(cdiv(K, 64));
+    s.k_sub = uint32_t(k_sub_now());
+    s.num_kb = int32_t(cdiv(K, int64_t(64) * s.k_sub));
     int pair = 1;
     {
         // Auto: the pair when its 256-row tiles waste at most ~10% more rows
@@ -601,15 +628,19 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
             std::lock_guard<std::mutex> lk(g_mu);
             forced = g_gemm_pair;
         }
-        const int max1 = umma_max_stages(1, c->smem_optin);
+        const int max1 = umma_max_stages(1, c->smem_optin, int(s.k_sub));
+        const int max2 = umma_max_stages(2, c->smem_optin, int(s.k_sub));
         if (forced == 1 && stages > max1)
             return fail(GBR_ERR_SMEM, "stages=%d exceeds %d for one CTA per tile", stages, max1);
         if (forced > 0)
             pair = forced;
         else
             pair = (stages > max1 || (maxn > 128 && rows2 * 10 <= rows1 * 11)) ? 2 : 1;
+        if (pair == 2 && stages > max2)
+            return fail(GBR_ERR_SMEM, "stages=%d exceeds %d for this stage size", stages, max2);
     }
     s.group_m = group_m_for(pair);
+    s.l2_hint = l2_hint_now();
     GroupTable g;
     memset(&g, 0, sizeof(g));
     g.num_groups = num_groups;
@@ -654,7 +685,7 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
         mw = mc[last_valid];
     }
     if ((r = check_umma_regs(*c, kUmmaBf16, true, pair)) != GBR_OK) return r;
-    const size_t smem = umma_smem_bytes(stages, pair);
+    const size_t smem = umma_smem_bytes(stages, pair, int(s.k_sub));
     cudaError_t e = umma_prepare(kUmmaBf16, true, pair, smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(grouped GEMM)");
     const int grid = pair * int(std::min<int64_t>(s.num_tiles, c->sm_count / pair));

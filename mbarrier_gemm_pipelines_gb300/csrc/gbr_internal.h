@@ -39,6 +39,10 @@ struct GemmShape {
     const float* bias;
     void* C;                       // used by epilogues that store with st.global
     KernelCtl ctl;
+    uint32_t k_sub;                // tensor-core GEMM: 128-byte K slices per ring stage (1, 2)
+    uint32_t l2_hint;              // tensor-core GEMM operand loads: 0 none, 1 A and B
+                                   // evict_last, 2 A evict_first / B evict_last,
+                                   // 3 A evict_last / B evict_first, 4 both evict_normal
 };
 
 // FFMA path (strict fp32, CUDA cores): 128x128x32 tiles.
@@ -71,8 +75,8 @@ struct GroupTable {
 
 // pair = 1: one CTA per 128x256 tile; pair = 2: a two-CTA cluster per 256x256
 // tile (cta_group::2).  Overloads without `pair` mean pair = 1.
-size_t umma_ring_bytes(int stages, int pair);    // shared memory the ring needs
-size_t umma_smem_bytes(int stages, int pair);    // what the launch requests
+size_t umma_ring_bytes(int stages, int pair, int k_sub = 1);   // shared memory the ring needs
+size_t umma_smem_bytes(int stages, int pair, int k_sub = 1);   // what the launch requests
 size_t umma_smem_bytes(int stages);
 cudaError_t umma_prepare(int kind, bool grouped, int pair, size_t smem);
 cudaError_t umma_prepare(int kind, bool grouped, size_t smem);

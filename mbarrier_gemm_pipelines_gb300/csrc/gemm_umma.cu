@@ -118,6 +118,32 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
            (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
 
+// TMA loads of one operand box, one CTA or the CTA pair, with or without an
+// L2 eviction-priority policy.
+template <int PAIR>
+__device__ __forceinline__ void load_box_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t c0, int32_t c1, bool hint, uint64_t pol) {
+    if (PAIR == 2) {
+        if (hint) ptx::tma_load_2d_pair_hint(dst, map, bar, c0, c1, pol);
+        else ptx::tma_load_2d_pair(dst, map, bar, c0, c1);
+    } else {
+        if (hint) ptx::tma_load_2d_hint(dst, map, bar, c0, c1, pol);
+        else ptx::tma_load_2d(dst, map, bar, c0, c1);
+    }
+}
+template <int PAIR>
+__device__ __forceinline__ void load_box_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2, bool hint,
+                                            uint64_t pol) {
+    if (PAIR == 2) {
+        if (hint) ptx::tma_load_3d_pair_hint(dst, map, bar, c0, c1, c2, pol);
+        else ptx::tma_load_3d_pair(dst, map, bar, c0, c1, c2);
+    } else {
+        if (hint) ptx::tma_load_3d_hint(dst, map, bar, c0, c1, c2, pol);
+        else ptx::tma_load_3d(dst, map, bar, c0, c1, c2);
+    }
+}
+
 template <bool GROUPED>
 struct UmmaParams {
     CUtensorMap mapA;
@@ -134,6 +160,8 @@ struct TileInfo {
     int32_t n0;      // first output column of the tile
     int32_t group;
 };
+
+__device__ __forceinline__ uint32_t s_ksub(const GemmShape& s) { return s.k_sub == 2 ? 2u : 1u; }
 
 template <bool GROUPED, int PAIR>
 __device__ __forceinline__ TileInfo decode_tile(const UmmaParams<GROUPED>& P, uint32_t t,
@@ -172,7 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* base = align_1024(smem_raw);
     const int S = P.s.stages;
     uint8_t* ring = base;
-    uint8_t* epi = ring + size_t(S) * PR::stage_bytes;
+    const uint32_t ksub = s_ksub(P.s);                   // 128-byte K slices per stage
+    const uint32_t stage_bytes = ksub * PR::stage_bytes; // [ksub A slices][ksub B slices]
+    uint8_t* epi = ring + size_t(S) * stage_bytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(epi + kUmmaEpiBytes);
     uint64_t* empty = full + S;
     uint64_t* acc_full = empty + S;
@@ -224,6 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------- TMA producer
             const uint32_t ring_base = ptx::smem_addr(ring);
+            const bool hint = s.l2_hint != 0;
+            const uint64_t pol_last = ptx::l2_policy_evict_last();
+            const uint64_t pol_first = ptx::l2_policy_evict_first();
+            const uint64_t pol_normal = ptx::l2_policy_evict_normal();
+            const uint64_t pol_a = s.l2_hint == 2 ? pol_first : s.l2_hint == 4 ? pol_normal : pol_last;
+            const uint64_t pol_b = s.l2_hint == 3 ? pol_first : s.l2_hint == 4 ? pol_normal : pol_last;
             uint32_t it = 0;
             bool ok = true;
             for (uint32_t t = unit; ok && t < uint32_t(s.num_tiles); t += units) {
@@ -238,35 +274,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t fb_local = ptx::smem_addr(full + slot);
                     const uint32_t fb = PAIR == 2 ? ptx::mapa_shared(fb_local, 0) : fb_local;
-                    if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, PAIR * PR::stage_bytes);
-                    const uint32_t a_dst = ring_base + slot * PR::stage_bytes;
-                    const uint32_t b_dst = a_dst + kUmmaAStageBytes;
-                    const int32_t k0 = kb * int32_t(K_::bk);
-                    if (PAIR == 2)
-                        ptx::tma_load_2d_pair(a_dst, &P.mapA, fb, k0, ti.a_row);
-                    else
-                        ptx::tma_load_2d(a_dst, &P.mapA, fb, k0, ti.a_row);
-                    if (K_::b_kmajor) {
-                        // Bt[N, K]: one box of this CTA's b_cols rows, 128 bytes of K each.
-                        if (PAIR == 2)
-                            ptx::tma_load_2d_pair(b_dst, &P.mapB, fb, k0, bcol0);
-                        else
-                            ptx::tma_load_2d(b_dst, &P.mapB, fb, k0, bcol0);
-                    } else {
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, PAIR * stage_bytes);
+                    const uint32_t stage_base = ring_base + slot * stage_bytes;
+                    for (uint32_t h = 0; h < ksub; ++h) {
+                        const uint32_t a_dst = stage_base + h * kUmmaAStageBytes;
+                        const uint32_t b_dst =
+                            stage_base + ksub * kUmmaAStageBytes + h * PR::b_bytes;
+                        const int32_t k0 = (kb * int32_t(ksub) + int32_t(h)) * int32_t(K_::bk);
+                        load_box_2d<PAIR>(a_dst, &P.mapA, fb, k0, ti.a_row, hint, pol_a);
+                        if (K_::b_kmajor) {
+                            // Bt[N, K]: one box of this CTA's b_cols rows, 128 bytes of K each.
+                            load_box_2d<PAIR>(b_dst, &P.mapB, fb, k0, bcol0, hint, pol_b);
+                        } else {
 #pragma unroll
-                        for (uint32_t j = 0; j < PR::b_cols / K_::panel_cols; ++j) {
-                            const int32_t n = bcol0 + int32_t(j * K_::panel_cols);
-                            const uint32_t d = b_dst + j * kPanelBytes;
-                            if (GROUPED) {
-                                if (PAIR == 2)
-                                    ptx::tma_load_3d_pair(d, &P.mapB, fb, n, k0, ti.group);
+                            for (uint32_t j = 0; j < PR::b_cols / K_::panel_cols; ++j) {
+                                const int32_t n = bcol0 + int32_t(j * K_::panel_cols);
+                                const uint32_t d = b_dst + j * kPanelBytes;
+                                if (GROUPED)
+                                    load_box_3d<PAIR>(d, &P.mapB, fb, n, k0, ti.group, hint, pol_b);
                                 else
-                                    ptx::tma_load_3d(d, &P.mapB, fb, n, k0, ti.group);
-                            } else {
-                                if (PAIR == 2)
-                                    ptx::tma_load_2d_pair(d, &P.mapB, fb, n, k0);
-                                else
-                                    ptx::tma_load_2d(d, &P.mapB, fb, n, k0);
+                                    load_box_2d<PAIR>(d, &P.mapB, fb, n, k0, hint, pol_b);
                             }
                         }
                     }
@@ -297,8 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    const uint32_t a_base = ring_base + slot * PR::stage_bytes;
-                    const uint32_t b_base = a_base + kUmmaAStageBytes;
+                    const uint32_t stage_base = ring_base + slot * stage_bytes;
+                    for (uint32_t h = 0; h < ksub; ++h) {
+                    const uint32_t a_base = stage_base + h * kUmmaAStageBytes;
+                    const uint32_t b_base = stage_base + ksub * kUmmaAStageBytes + h * PR::b_bytes;
 #pragma unroll
                     for (uint32_t k = 0; k < 128 / (K_::mma_k * K_::esize); ++k) {
                         const uint64_t ad = sw128_desc(a_base + k * K_::mma_k * K_::esize, 16, 1024);
@@ -306,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             K_::b_kmajor
                                 ? sw128_desc(b_base + k * K_::mma_k * K_::esize, 16, 1024)
                                 : sw128_desc(b_base + k * K_::mma_k * 128, kPanelBytes, 1024);
-                        const uint32_t acc = (kb | k) != 0;
+                        const uint32_t acc = (uint32_t(kb) | h | k) != 0;
                         if (PAIR == 2) {
                             if (KIND == kUmmaBf16)
                                 ptx::mma_f16_pair(d_tmem, ad, bd, kIdesc, acc);
@@ -318,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             else
                                 ptx::mma_tf32(d_tmem, ad, bd, kIdesc, acc);
                         }
+                    }
                     }
                     if (PAIR == 2)
                         ptx::mma_commit_pair_multicast(ptx::smem_addr(empty + slot), 0x3);
@@ -508,13 +538,13 @@ cudaError_t launch_pair(int kind, const UmmaParams<GROUPED>& P, int grid, size_t
 
 }  // namespace
 
-size_t umma_ring_bytes(int stages, int pair) {
+size_t umma_ring_bytes(int stages, int pair, int k_sub) {
     const size_t stage = pair == 2 ? Pair<2>::stage_bytes : Pair<1>::stage_bytes;
-    return 1024 + size_t(stages) * stage + kUmmaEpiBytes + 256;
+    return 1024 + size_t(stages) * size_t(k_sub) * stage + kUmmaEpiBytes + 256;
 }
 
-size_t umma_smem_bytes(int stages, int pair) {
-    const size_t need = umma_ring_bytes(stages, pair);
+size_t umma_smem_bytes(int stages, int pair, int k_sub) {
+    const size_t need = umma_ring_bytes(stages, pair, k_sub);
     // At least half the SM's shared memory, so that two CTAs never share an
     // SM and compete for its 512 TMEM columns.
     const size_t floor_one_cta = 120 * 1024;

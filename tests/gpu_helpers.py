@@ -58,13 +58,13 @@ class tuned:
     """Forces the tensor-core GEMM variant (1: one CTA per tile, 2: CTA pair)
     for the duration of a with-block, then restores the automatic choice."""
 
-    def __init__(self, gbr, pair):
-        self.gbr, self.pair = gbr, pair
+    def __init__(self, gbr, pair, k_per_stage=-1):
+        self.gbr, self.pair, self.ks = gbr, pair, k_per_stage
 
     def __enter__(self):
-        self.gbr.gemm_tuning(self.pair, -1)
+        self.gbr.gemm_tuning(self.pair, -1, -1, self.ks)
         return self
 
     def __exit__(self, *exc):
-        self.gbr.gemm_tuning(-1, -1)
+        self.gbr.gemm_tuning(-1, -1, -1, -1)
         return False

@@ -66,8 +66,11 @@ def test_small_shapes(gbr, dtype, pair, M, N, K):
     _check_full(got, A.float(), B.float(), bias, dtype)
 
 
-@pytest.mark.parametrize("dtype,pair", VARIANTS)
-def test_stage_sweep(gbr, dtype, pair):
+@pytest.mark.parametrize("dtype,pair,ks", [v + (1,) for v in VARIANTS] +
+                         [("tf32", 1, 2), ("tf32", 2, 2), ("bf16", 1, 2), ("bf16", 2, 2)])
+def test_stage_sweep(gbr, dtype, pair, ks):
+    """Every ring depth, one CTA or a pair per tile, one or two 128-byte K
+    slices per stage (K = 640 leaves a ragged last stage in both)."""
     M, N, K = 384, 512, 640
     A, B, bias = inputs.gemm_normal(M, N, K, seed=5)
     if dtype == "bf16":
@@ -76,7 +79,9 @@ def test_stage_sweep(gbr, dtype, pair):
     assert smax >= 4
     if pair == 1:
         smax = 4                                   # one CTA per tile holds 4 stages
-    with tuned(gbr, pair):
+    if ks == 2:
+        smax = 2 if pair == 1 else 3               # stages twice as large
+    with tuned(gbr, pair, ks):
         for S in range(1, smax + 1):
             got = _run(gbr, A, B, bias, dtype, S)
             _check_full(got, A.float(), B.float(), bias, dtype)
@@ -207,11 +212,13 @@ def test_config3_fp32_4096(gbr, dtype, S, pair):
         _sampled(gbr, A, B, bias, dtype, S, 3000, seed=2)
 
 
-@pytest.mark.parametrize("S,pair", [(4, -1), (5, -1), (6, -1), (4, 1)])
-def test_config4_bf16_8192(gbr, S, pair):
-    """bf16 8192^3, 4-6 stage ring (the pair kernel by default; one CTA per tile at S=4)."""
+@pytest.mark.parametrize("S,pair,ks", [(4, -1, -1), (5, -1, -1), (6, -1, -1), (4, 1, -1),
+                                        (3, 2, 2)])
+def test_config4_bf16_8192(gbr, S, pair, ks):
+    """bf16 8192^3, 4-6 stage ring (the pair kernel by default; one CTA per tile
+    at S=4; 3 stages of 128 K = 6 x 64 K)."""
     A, B, bias = inputs.workload("gemm_bf16")
-    with tuned(gbr, pair):
+    with tuned(gbr, pair, ks):
         C = _sampled(gbr, A, B, bias, "bf16", S, 3000, seed=3)
     assert bool((C >= 0).all())
 

@@ -72,12 +72,12 @@ def test_grouped_rejects(gbr):
                                             bnd.BF16, 2, None) == bnd.ERR_INVALID
 
 
-@pytest.mark.parametrize("pair,S", [(-1, 4), (1, 4), (2, 6)])
-def test_config5_moe_sampled(gbr, pair, S):
+@pytest.mark.parametrize("pair,S,ks", [(-1, 4, -1), (1, 4, -1), (2, 6, -1), (1, 2, 2), (2, 3, 2)])
+def test_config5_moe_sampled(gbr, pair, S, ks):
     """4096 tokens over 8 experts (Multinomial counts, seed 4), K = 4096,
     N = 14336, one launch; sampled positions in every expert."""
     counts, X, W, b = inputs.workload("grouped_bf16")
-    with tuned(gbr, pair):
+    with tuned(gbr, pair, ks):
         C = gbr.gemm_bias_relu_grouped(X.cuda(), W.cuda(), b.cuda(), counts, stages=S)
     gbr.check_device()
     T, N = C.shape
