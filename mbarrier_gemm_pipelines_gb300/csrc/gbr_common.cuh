@@ -48,6 +48,12 @@ __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
     return CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
 }
 
+// Non-blocking poll (never suspends the thread).
+template <bool CLUSTER>
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    return CLUSTER ? ptx::mbar_test_wait_cluster(bar, parity) : ptx::mbar_test_wait(bar, parity);
+}
+
 // Slow path of a bounded wait: polls until the phase completes, another role
 // raised the CTA's abort flag, or the time/iteration limit runs out (then it
 // records the site, raises the abort flag and gives up).

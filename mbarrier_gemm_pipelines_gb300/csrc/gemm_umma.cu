@@ -161,8 +161,6 @@ struct TileInfo {
     int32_t group;
 };
 
-__device__ __forceinline__ uint32_t s_ksub(const GemmShape& s) { return s.k_sub == 2 ? 2u : 1u; }
-
 template <bool GROUPED, int PAIR>
 __device__ __forceinline__ TileInfo decode_tile(const UmmaParams<GROUPED>& P, uint32_t t,
                                                 uint32_t rank) {
@@ -186,7 +184,7 @@ __device__ __forceinline__ TileInfo decode_tile(const UmmaParams<GROUPED>& P, ui
     return ti;
 }
 
-template <int KIND, bool GROUPED, int PAIR>
+template <int KIND, bool GROUPED, int PAIR, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_umma_kernel(const __grid_constant__ UmmaParams<GROUPED> P) {
     using K_ = Kind<KIND>;
@@ -200,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* base = align_1024(smem_raw);
     const int S = P.s.stages;
     uint8_t* ring = base;
-    const uint32_t ksub = s_ksub(P.s);                   // 128-byte K slices per stage
-    const uint32_t stage_bytes = ksub * PR::stage_bytes; // [ksub A slices][ksub B slices]
+    constexpr uint32_t ksub = KSUB;                      // 128-byte K slices per stage
+    constexpr uint32_t stage_bytes = ksub * PR::stage_bytes;  // [ksub A slices][ksub B slices]
     uint8_t* epi = ring + size_t(S) * stage_bytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(epi + kUmmaEpiBytes);
     uint64_t* empty = full + S;
@@ -276,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb = PAIR == 2 ? ptx::mapa_shared(fb_local, 0) : fb_local;
                     if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, PAIR * stage_bytes);
                     const uint32_t stage_base = ring_base + slot * stage_bytes;
+#pragma unroll
                     for (uint32_t h = 0; h < ksub; ++h) {
                         const uint32_t a_dst = stage_base + h * kUmmaAStageBytes;
                         const uint32_t b_dst =
@@ -325,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::tc_fence_after_sync();
                     const uint32_t stage_base = ring_base + slot * stage_bytes;
+#pragma unroll
                     for (uint32_t h = 0; h < ksub; ++h) {
                     const uint32_t a_base = stage_base + h * kUmmaAStageBytes;
                     const uint32_t b_base = stage_base + ksub * kUmmaAStageBytes + h * PR::b_bytes;
@@ -500,24 +500,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int KIND, bool GROUPED, int PAIR>
+template <int KIND, bool GROUPED, int PAIR, int KSUB>
 void* kernel_ptr() {
-    return reinterpret_cast<void*>(&gemm_umma_kernel<KIND, GROUPED, PAIR>);
+    return reinterpret_cast<void*>(&gemm_umma_kernel<KIND, GROUPED, PAIR, KSUB>);
 }
 
-void* select_kernel(int kind, bool grouped, int pair) {
-    if (pair == 2) {
-        if (kind == kUmmaBf16)
-            return grouped ? kernel_ptr<kUmmaBf16, true, 2>() : kernel_ptr<kUmmaBf16, false, 2>();
-        return grouped ? kernel_ptr<kUmmaTf32, true, 2>() : kernel_ptr<kUmmaTf32, false, 2>();
-    }
+template <int KIND, bool GROUPED>
+void* select_kernel_kg(int pair, int ksub) {
+    if (pair == 2)
+        return ksub == 2 ? kernel_ptr<KIND, GROUPED, 2, 2>() : kernel_ptr<KIND, GROUPED, 2, 1>();
+    return ksub == 2 ? kernel_ptr<KIND, GROUPED, 1, 2>() : kernel_ptr<KIND, GROUPED, 1, 1>();
+}
+
+void* select_kernel(int kind, bool grouped, int pair, int ksub) {
     if (kind == kUmmaBf16)
-        return grouped ? kernel_ptr<kUmmaBf16, true, 1>() : kernel_ptr<kUmmaBf16, false, 1>();
-    return grouped ? kernel_ptr<kUmmaTf32, true, 1>() : kernel_ptr<kUmmaTf32, false, 1>();
+        return grouped ? select_kernel_kg<kUmmaBf16, true>(pair, ksub)
+                       : select_kernel_kg<kUmmaBf16, false>(pair, ksub);
+    return grouped ? select_kernel_kg<kUmmaTf32, true>(pair, ksub)
+                   : select_kernel_kg<kUmmaTf32, false>(pair, ksub);
 }
 
+int ksub_of(const GemmShape& s) { return s.k_sub == 2 ? 2 : 1; }
+
+// Launches the instance for (kind, pair, k_sub); a CTA pair is a cluster of 2.
 template <bool GROUPED>
-cudaError_t launch_pair(int kind, const UmmaParams<GROUPED>& P, int grid, size_t smem,
+cudaError_t launch_umma(int kind, int pair, const UmmaParams<GROUPED>& P, int grid, size_t smem,
                         cudaStream_t stream) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
@@ -527,13 +534,13 @@ cudaError_t launch_pair(int kind, const UmmaParams<GROUPED>& P, int grid, size_t
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = pair;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pair == 2 ? 1 : 0;
     void* args[] = {const_cast<UmmaParams<GROUPED>*>(&P)};
-    return cudaLaunchKernelExC(&cfg, select_kernel(kind, GROUPED, 2), args);
+    return cudaLaunchKernelExC(&cfg, select_kernel(kind, GROUPED, pair, ksub_of(P.s)), args);
 }
 
 }  // namespace
@@ -553,8 +560,13 @@ size_t umma_smem_bytes(int stages, int pair, int k_sub) {
 size_t umma_smem_bytes(int stages) { return umma_smem_bytes(stages, 1); }
 
 cudaError_t umma_prepare(int kind, bool grouped, int pair, size_t smem) {
-    return cudaFuncSetAttribute(select_kernel(kind, grouped, pair),
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    for (int ksub = 1; ksub <= 2; ++ksub) {
+        const cudaError_t e = cudaFuncSetAttribute(select_kernel(kind, grouped, pair, ksub),
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   int(smem));
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 cudaError_t umma_prepare(int kind, bool grouped, size_t smem) {
     return umma_prepare(kind, grouped, 1, smem);
@@ -562,11 +574,14 @@ cudaError_t umma_prepare(int kind, bool grouped, size_t smem) {
 
 cudaError_t umma_check_registers(int kind, bool grouped, int pair, int* regs) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, select_kernel(kind, grouped, pair));
-    if (e != cudaSuccess) return e;
-    *regs = fa.numRegs;
     const long need = 128L * kRegsWG0 + 128L * kRegsWG1;
-    return (long(fa.numRegs) * kThreads >= need) ? cudaSuccess : cudaErrorInvalidConfiguration;
+    for (int ksub = 1; ksub <= 2; ++ksub) {
+        cudaError_t e = cudaFuncGetAttributes(&fa, select_kernel(kind, grouped, pair, ksub));
+        if (e != cudaSuccess) return e;
+        *regs = fa.numRegs;
+        if (long(fa.numRegs) * kThreads < need) return cudaErrorInvalidConfiguration;
+    }
+    return cudaSuccess;
 }
 cudaError_t umma_check_registers(int kind, bool grouped, int* regs) {
     return umma_check_registers(kind, grouped, 1, regs);
@@ -582,12 +597,7 @@ cudaError_t launch_gemm_umma(int kind, int pair, const CUtensorMap& mapA, const 
     P.mapC[0] = mapC;
     P.s = s;
     P.bias_group_stride = 0;
-    if (pair == 2) return launch_pair<false>(kind, P, grid, smem, stream);
-    if (kind == kUmmaBf16)
-        gemm_umma_kernel<kUmmaBf16, false, 1><<<grid, kThreads, smem, stream>>>(P);
-    else
-        gemm_umma_kernel<kUmmaTf32, false, 1><<<grid, kThreads, smem, stream>>>(P);
-    return cudaGetLastError();
+    return launch_umma<false>(kind, pair, P, grid, smem, stream);
 }
 cudaError_t launch_gemm_umma(int kind, const CUtensorMap& mapA, const CUtensorMap& mapB,
                              const CUtensorMap& mapC, const GemmShape& s, int grid, size_t smem,
@@ -607,9 +617,7 @@ cudaError_t launch_gemm_umma_grouped(int pair, const CUtensorMap& mapX, const CU
     P.s = s;
     P.g = g;
     P.bias_group_stride = bias_group_stride;
-    if (pair == 2) return launch_pair<true>(kUmmaBf16, P, grid, smem, stream);
-    gemm_umma_kernel<kUmmaBf16, true, 1><<<grid, kThreads, smem, stream>>>(P);
-    return cudaGetLastError();
+    return launch_umma<true>(kUmmaBf16, pair, P, grid, smem, stream);
 }
 
 }  // namespace gbr
