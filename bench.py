@@ -310,6 +310,7 @@ def run_ours(args):
 
     M = N = K = 8192
     S = args.stages
+    gbr.gemm_tuning(args.pair, -1)
     A, B, bias = inputs.workload("gemm_bf16")
     dA, dB, dbias = A.to(dev), B.to(dev), bias.to(dev)
     dC = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -355,6 +356,7 @@ def run_ours(args):
     h2d = hA.numel() * 2 + hB.numel() * 2 + hbias.numel() * 4
     d2h = hC.numel() * 2
 
+    gbr.gemm_tuning(-1, -1)
     copy = measure_copy(gbr, peaks) if rank == 0 else None
     others = None
     if rank == 0 and not args.quick:
@@ -378,8 +380,9 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": "bf16 GEMM+bias+ReLU M=N=K=8192, A,B~N(0,1)/sqrt(K)->bf16, "
-                               "bias f32~N(0,0.1), seed 3; persistent 128x256x64 tiles, "
-                               "%d-stage TMA/mbarrier ring, tcgen05 MMA into TMEM" % S,
+                               "bias f32~N(0,0.1), seed 3; persistent CTA pairs (cta_group::2), "
+                               "256x256 tile per pair, %d-stage TMA/mbarrier ring "
+                               "(128 of K per stage when S<=3, else 64), tcgen05 MMA into TMEM" % S,
                    "M": M, "N": N, "K": K, "stages": S,
                    "l2": "inputs larger than L2 (A+B = 256 MiB > 129 MB); no flush",
                    "parallelism": "replica per GPU" if world > 1 else "single GPU"},
@@ -438,7 +441,7 @@ def run_reference(args):
     emit(res)
 
 
-def run_profile_case(case, launches=2):
+def run_profile_case(case, launches=2, stages=4, pair=-1):
     """A short fixed invocation for Nsight Compute: `launches` launches of one
     kernel on its workload, nothing timed, nothing printed but a status line."""
     import torch
@@ -446,10 +449,11 @@ def run_profile_case(case, launches=2):
     from mbarrier_gemm_pipelines_gb300 import inputs
     gbr.build()
     torch.cuda.set_device(0)
+    gbr.gemm_tuning(pair, -1)
     if case == "copy":
         src = inputs.workload("copy").cuda()
         dst = torch.empty_like(src)
-        fn = lambda: gbr.staged_copy(src, dst, tile=(128, 64), stages=4)
+        fn = lambda: gbr.staged_copy(src, dst, tile=(128, 64), stages=stages)
     elif case in ("gemm_bf16", "gemm_tf32", "gemm_ffma"):
         if case == "gemm_bf16":
             A, B, bias = inputs.workload("gemm_bf16")
@@ -457,11 +461,11 @@ def run_profile_case(case, launches=2):
             A, B, bias = inputs.workload("gemm_fp32")
         dA, dB, db = A.cuda(), B.cuda(), bias.cuda()
         dt = case.split("_")[1]
-        fn = lambda: gbr.gemm_bias_relu(dA, dB, db, dtype=dt, stages=4)
+        fn = lambda: gbr.gemm_bias_relu(dA, dB, db, dtype=dt, stages=stages)
     elif case == "grouped":
         counts, X, W, b = inputs.workload("grouped_bf16")
         dX, dW, db = X.cuda(), W.cuda(), b.cuda()
-        fn = lambda: gbr.gemm_bias_relu_grouped(dX, dW, db, counts, stages=4)
+        fn = lambda: gbr.gemm_bias_relu_grouped(dX, dW, db, counts, stages=stages)
     else:
         raise SystemExit("unknown profile case %r" % case)
     for _ in range(launches):
@@ -475,7 +479,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--stages", type=int, default=4)
+    ap.add_argument("--stages", type=int, default=3)
+    ap.add_argument("--pair", type=int, default=-1, choices=[-1, 1, 2],
+                    help="tensor-core GEMM variant: -1 auto, 1 one CTA per tile, 2 CTA pair")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -486,7 +492,7 @@ def main():
                          "gemm_ffma or grouped")
     args = ap.parse_args()
     if args.profile:
-        run_profile_case(args.profile)
+        run_profile_case(args.profile, stages=args.stages, pair=args.pair)
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

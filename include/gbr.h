@@ -77,7 +77,8 @@ typedef enum {
  *   stages  ring depth S, 1 <= S <= gbr_max_stages(GBR_OP_GEMM, dtype, 0, 0)
  *         (GBR_ERR_SMEM otherwise).  Tiles: FFMA 128x128x32 fp32;
  *         tcgen05 128x256 per CTA, or 256x256 per CTA pair (gbr_gemm_tuning),
- *         with 128 bytes of K per stage (bf16 K=64, tf32 K=32).
+ *         with 128 bytes of K per stage (bf16 K=64, tf32 K=32), or 256 bytes
+ *         when S <= 3 on the CTA pair (bf16 K=128, tf32 K=64).
  *   stream  see above.
  * Ragged M, N and K need no padding: TMA loads zero-fill outside the tensor
  * and TMA stores drop rows/columns outside it.
@@ -177,9 +178,10 @@ int gbr_copy_tuning(int store_lag, int ctas_per_sm);
  * rows).  group_m: -1 auto, else output-tile rows per raster band.
  * l2_hint: L2 eviction priority of the A/B tile loads: -1 auto (none), 0 none,
  * 1 both evict_last, 2 A evict_first + B evict_last, 3 A evict_last + B
- * evict_first, 4 both evict_normal.  k_per_stage: -1 auto (1), 1 or 2 slices
- * of 128 bytes of K per ring stage; with 2 a stage is twice as large (so the
- * largest `stages` halves) and each full/empty handshake covers twice the MMAs.
+ * evict_first, 4 both evict_normal.  k_per_stage: 1 or 2 slices of 128 bytes
+ * of K per ring stage; with 2 a stage is twice as large (so the largest
+ * `stages` halves) and each full/empty handshake covers twice the MMAs; -1
+ * auto: 2 on the CTA pair whenever `stages` fits (<= 3), else 1.
  */
 int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage);
 

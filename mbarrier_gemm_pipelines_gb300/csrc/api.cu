@@ -175,9 +175,18 @@ int umma_max_stages(int pair, int smem_optin, int k_sub = 1) {
     return max_stages_for(pair == 2 ? umma2_bytes_fn : umma1_bytes_fn, smem_optin);
 }
 
-int k_sub_now() {
+int k_sub_forced() {
     std::lock_guard<std::mutex> lk(g_mu);
-    return g_gemm_k_sub == 2 ? 2 : 1;
+    return g_gemm_k_sub;
+}
+
+// 128-byte K slices per stage: forced by gbr_gemm_tuning, else two on the
+// CTA pair whenever the requested ring fits (fewer full/empty handshakes per
+// MMA; the handshakes, not the loads, limit the one-slice ring).
+int choose_k_sub(int pair, int stages, int smem_optin) {
+    const int f = k_sub_forced();
+    if (f == 1 || f == 2) return f;
+    return (pair == 2 && stages <= umma_max_stages(2, smem_optin, 2)) ? 2 : 1;
 }
 
 // Largest ring depth for the dtype (tcgen05: that of the CTA-pair kernel).
@@ -195,9 +204,9 @@ int choose_pair(int64_t rows, int stages, int smem_optin, int* pair) {
         std::lock_guard<std::mutex> lk(g_mu);
         forced = g_gemm_pair;
     }
-    const int ks = k_sub_now();
+    const int fk = k_sub_forced();
+    const int ks = fk == 2 ? 2 : 1;   // pair choice is made for the smaller stage unless forced
     const int max1 = umma_max_stages(1, smem_optin, ks);
-    const int max2 = umma_max_stages(2, smem_optin, ks);
     if (forced == 1) {
         if (stages > max1)
             return fail(GBR_ERR_SMEM, "stages=%d exceeds %d for one CTA per tile", stages, max1);
@@ -207,6 +216,7 @@ int choose_pair(int64_t rows, int stages, int smem_optin, int* pair) {
     } else {
         *pair = (rows > 128 || stages > max1) ? 2 : 1;
     }
+    const int max2 = umma_max_stages(2, smem_optin, ks);
     if (*pair == 2 && stages > max2)
         return fail(GBR_ERR_SMEM, "stages=%d exceeds %d for this stage size", stages, max2);
     return GBR_OK;
@@ -511,7 +521,7 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
     const uint32_t panel_cols = uint32_t(128 / es);  // B panel width; also the C store box width
     int pair = 1;
     if ((r = choose_pair(M, stages, c->smem_optin, &pair)) != GBR_OK) return r;
-    s.k_sub = uint32_t(k_sub_now());
+    s.k_sub = uint32_t(choose_k_sub(pair, stages, c->smem_optin));
     s.m_tiles = int32_t(cdiv(M, int64_t(kUmmaBM) * pair));
     s.n_tiles = int32_t(cdiv(N, kUmmaBN));
     s.num_kb = int32_t(cdiv(K, int64_t(bk) * s.k_sub));
@@ -611,8 +621,7 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
     s.C = C;
     s.ctl = make_ctl(*c);
     s.n_tiles = int32_t(cdiv(N, kUmmaBN));
-    s.k_sub = uint32_t(k_sub_now());
-    s.num_kb = int32_t(cdiv(K, int64_t(64) * s.k_sub));
+    s.k_sub = uint32_t(k_sub_forced() == 2 ? 2 : 1);
     int pair = 1;
     {
         // Auto: the pair when its 256-row tiles waste at most ~10% more rows
@@ -638,7 +647,9 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
             pair = (stages > max1 || (maxn > 128 && rows2 * 10 <= rows1 * 11)) ? 2 : 1;
         if (pair == 2 && stages > max2)
             return fail(GBR_ERR_SMEM, "stages=%d exceeds %d for this stage size", stages, max2);
+        s.k_sub = uint32_t(choose_k_sub(pair, stages, c->smem_optin));
     }
+    s.num_kb = int32_t(cdiv(K, int64_t(64) * s.k_sub));
     s.group_m = group_m_for(pair);
     s.l2_hint = l2_hint_now();
     GroupTable g;

@@ -30,16 +30,6 @@ constexpr uint32_t kBPanelBytes = kFfmaBK * 128;      // 32 rows x 128 B
 constexpr uint32_t kProducerRegs = 40;
 constexpr uint32_t kConsumerRegs = 232;
 
-// Byte offset of A(m, k) inside a stage: 128-byte rows (32 fp32 of K), the
-// 16-byte chunk index XOR-ed with (m % 8) by the TMA 128-byte swizzle.
-__device__ __forceinline__ uint32_t a_off(uint32_t m, uint32_t k4) {
-    return m * 128u + ((k4 ^ (m & 7u)) << 4);
-}
-// Byte offset of B(k, n..n+3) (n % 4 == 0): 32-column panels of 32 rows.
-__device__ __forceinline__ uint32_t b_off(uint32_t k, uint32_t n) {
-    return (n >> 5) * kBPanelBytes + k * 128u + ((((n & 31u) >> 2) ^ (k & 7u)) << 4);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_ffma_kernel(const __grid_constant__ CUtensorMap mapA,
                      const __grid_constant__ CUtensorMap mapB, const GemmShape p) {
@@ -101,13 +91,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         ptx::setmaxnreg_inc<kConsumerRegs>();
         // ---------------------------------------------------- consumers
+        // Thread (tx, ty) of 16 x 16 owns rows ty + 16 r (r = 0..7) and columns
+        // 4 tx .. 4 tx + 3 and 64 + 4 tx .. 64 + 4 tx + 3 of the 128 x 128 tile.
+        // All its rows have the same (row % 8), so every A read of a k-group
+        // uses one swizzle phase; all its columns sit at the same position
+        // inside their 32-column panels, so every B read of a k uses one
+        // phase too.  The phases come from two 8-entry tables and every
+        // shared-memory load is base + immediate offset.
         const uint32_t ct = threadIdx.x - 128;        // 0..255
-        const uint32_t tx = ct & 15u, ty = ct >> 4;   // 16 x 16 threads
-        // Rows 4ty..4ty+3 and 64+4ty..; columns 4tx..4tx+3 and 64+4tx..
-        uint32_t a_row[8];
+        const uint32_t tx = ct & 15u, ty = ct >> 4;
+        uint32_t a_sw[8], b_sw[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) a_row[r] = (r < 4 ? 0u : 64u) + 4u * ty + (r & 3);
-        const uint32_t n_lo = 4u * tx, n_hi = 64u + 4u * tx;
+        for (uint32_t j = 0; j < 8; ++j) {
+            a_sw[j] = ty * 128u + ((j ^ (ty & 7u)) << 4);                 // row ty, chunk j
+            b_sw[j] = (tx >> 3) * kBPanelBytes + (((tx & 7u) ^ j) << 4);  // column 4 tx, K row % 8 = j
+        }
 
         uint32_t i = 0;
         bool ok = true;
@@ -129,17 +127,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint8_t* As = ring + size_t(s) * kFfmaStageBytes;
                 const uint8_t* Bs = As + kABytes;
-#pragma unroll 2
+#pragma unroll
                 for (uint32_t k4 = 0; k4 < kFfmaBK / 4; ++k4) {
+                    const uint8_t* ap = As + a_sw[k4];
                     float4 a[8];
 #pragma unroll
                     for (int r = 0; r < 8; ++r)
-                        a[r] = *reinterpret_cast<const float4*>(As + a_off(a_row[r], k4));
+                        a[r] = *reinterpret_cast<const float4*>(ap + r * 16 * 128);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t k = 4 * k4 + kk;
-                        const float4 b0 = *reinterpret_cast<const float4*>(Bs + b_off(k, n_lo));
-                        const float4 b1 = *reinterpret_cast<const float4*>(Bs + b_off(k, n_hi));
+                        const uint8_t* bp = Bs + b_sw[k & 7u] + k * 128u;
+                        const float4 b0 = *reinterpret_cast<const float4*>(bp);
+                        const float4 b1 = *reinterpret_cast<const float4*>(bp + 2 * kBPanelBytes);
                         const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
                         for (int r = 0; r < 8; ++r) {
@@ -160,12 +160,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n0 = int(nt) * kFfmaBN, m0 = int(mt) * kFfmaBM;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int n = n0 + int(h == 0 ? n_lo : n_hi);
+                const int n = n0 + int(4 * tx) + 64 * h;
                 if (n >= p.N) continue;
                 const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + n));
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
-                    const int m = m0 + int(a_row[r]);
+                    const int m = m0 + int(ty) + 16 * r;
                     if (m >= p.M) continue;
                     float4 v;
                     v.x = fmaxf(acc[r][4 * h + 0] + bb.x, 0.f);
