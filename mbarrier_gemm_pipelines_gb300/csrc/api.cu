@@ -6,7 +6,9 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <array>
 #include <atomic>
+#include <map>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -40,6 +42,32 @@ struct DevCtx {
     bool umma_regs_checked[2][2][2] = {};
 };
 DevCtx g_dev[kMaxDevices];
+
+// Per-device memo of launch preparation (raising a kernel's dynamic shared
+// memory limit, querying its occupancy): done once per (kernel, size), not on
+// every call.  Key: {operator, dtype/kind, grouped, pair, smem bytes}.
+using PrepKey = std::array<int64_t, 5>;
+std::mutex g_prep_mu;
+std::map<PrepKey, int> g_prep[kMaxDevices];
+
+template <class F>
+int prepared(int dev, const PrepKey& key, int* value, F&& prepare) {
+    {
+        std::lock_guard<std::mutex> lk(g_prep_mu);
+        auto it = g_prep[dev].find(key);
+        if (it != g_prep[dev].end()) {
+            *value = it->second;
+            return GBR_OK;
+        }
+    }
+    const int r = prepare(value);
+    if (r != GBR_OK) return r;
+    std::lock_guard<std::mutex> lk(g_prep_mu);
+    g_prep[dev][key] = *value;
+    return GBR_OK;
+}
+
+enum PrepOp : int64_t { kPrepCopy = 1, kPrepFfma = 2, kPrepUmma = 3 };
 
 int fail(int code, const char* fmt, ...) {
     char buf[512];
@@ -372,7 +400,8 @@ int staged_copy(const void* src, void* dst, int64_t rows, int64_t cols, int tile
         return fail(GBR_ERR_INVALID, "staged_copy: tile must be 1..256 x 4..256");
     if (tile_cols % 4) return fail(GBR_ERR_ALIGN, "staged_copy: tile_cols must be a multiple of 4");
     DevCtx* c;
-    int r = get_ctx(&c);
+    int dev = 0;
+    int r = get_ctx(&c, &dev);
     if (r != GBR_OK) return r;
     const uint32_t tile_bytes = uint32_t(tile_rows) * uint32_t(tile_cols) * 4u;
     const int smax = copy_max_stages(tile_bytes, c->smem_optin);
@@ -417,10 +446,16 @@ int staged_copy(const void* src, void* dst, int64_t rows, int64_t cols, int tile
     a.ctl = make_ctl(*c);
 
     const size_t smem = copy_smem_bytes(stages, tile_bytes);
-    cudaError_t e = copy_prepare(smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(staged copy)");
     int occ = 0;
-    if ((e = copy_occupancy(smem, &occ)) != cudaSuccess) return cuda_fail(e, "occupancy(staged copy)");
+    r = prepared(dev, {kPrepCopy, 0, 0, 0, int64_t(smem)}, &occ, [&](int* v) {
+        cudaError_t e2 = copy_prepare(smem);
+        if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFuncSetAttribute(staged copy)");
+        if ((e2 = copy_occupancy(smem, v)) != cudaSuccess)
+            return cuda_fail(e2, "occupancy(staged copy)");
+        return int(GBR_OK);
+    });
+    if (r != GBR_OK) return r;
+    cudaError_t e;
     if (occ < 1) return fail(GBR_ERR_SMEM, "staged_copy: kernel does not fit on an SM");
     if (cps > 0 && cps < occ) occ = cps;
     const int64_t grid = std::min<int64_t>(a.num_tiles, int64_t(c->sm_count) * occ);
@@ -438,7 +473,8 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
     if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim)
         return fail(GBR_ERR_INVALID, "gemm_bias_relu: M, N, K must be in [0, 2^31)");
     DevCtx* c;
-    int r = get_ctx(&c);
+    int dev = 0;
+    int r = get_ctx(&c, &dev);
     if (r != GBR_OK) return r;
     const int smax = gemm_max_stages(dtype, c->smem_optin);
     if (stages < 1 || stages > smax)
@@ -503,9 +539,14 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
                 return fail(GBR_ERR_CUDA, "FFMA GEMM kernel was built with too few registers for its role split");
         }
         const size_t smem = ffma_smem_bytes(stages);
-        if ((e = ffma_prepare(smem)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(FFMA)");
         int occ = 0;
-        if ((e = ffma_occupancy(smem, &occ)) != cudaSuccess) return cuda_fail(e, "occupancy(FFMA)");
+        r = prepared(dev, {kPrepFfma, 0, 0, 0, int64_t(smem)}, &occ, [&](int* v) {
+            cudaError_t e2 = ffma_prepare(smem);
+            if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFuncSetAttribute(FFMA)");
+            if ((e2 = ffma_occupancy(smem, v)) != cudaSuccess) return cuda_fail(e2, "occupancy(FFMA)");
+            return int(GBR_OK);
+        });
+        if (r != GBR_OK) return r;
         if (occ < 1) return fail(GBR_ERR_SMEM, "FFMA GEMM does not fit on an SM");
         const int grid = int(std::min<int64_t>(s.num_tiles, int64_t(c->sm_count) * occ));
         if ((e = launch_gemm_ffma(ma, mb, s, grid, smem, st)) != cudaSuccess)
@@ -534,8 +575,14 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
         return r;
     if ((r = check_umma_regs(*c, kind, false, pair)) != GBR_OK) return r;
     const size_t smem = umma_smem_bytes(stages, pair, int(s.k_sub));
-    if ((e = umma_prepare(kind, false, pair, smem)) != cudaSuccess)
-        return cuda_fail(e, "cudaFuncSetAttribute(tcgen05 GEMM)");
+    int one = 0;
+    r = prepared(dev, {kPrepUmma, kind, 0, pair, int64_t(smem)}, &one, [&](int* v) {
+        const cudaError_t e2 = umma_prepare(kind, false, pair, smem);
+        if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFuncSetAttribute(tcgen05 GEMM)");
+        *v = 1;
+        return int(GBR_OK);
+    });
+    if (r != GBR_OK) return r;
     const int grid = pair * int(std::min<int64_t>(s.num_tiles, c->sm_count / pair));
     float* bt = nullptr;  // TF32 only: K-major copy of B, stream-ordered scratch
     if (K > 0) {
@@ -592,7 +639,8 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
     }
     if (T >= lim) return fail(GBR_ERR_INVALID, "gemm_bias_relu_grouped: too many rows");
     DevCtx* c;
-    int r = get_ctx(&c);
+    int dev = 0;
+    int r = get_ctx(&c, &dev);
     if (r != GBR_OK) return r;
     const int smax = gemm_max_stages(dtype, c->smem_optin);
     if (stages < 1 || stages > smax)
@@ -697,8 +745,15 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
     }
     if ((r = check_umma_regs(*c, kUmmaBf16, true, pair)) != GBR_OK) return r;
     const size_t smem = umma_smem_bytes(stages, pair, int(s.k_sub));
-    cudaError_t e = umma_prepare(kUmmaBf16, true, pair, smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(grouped GEMM)");
+    int one = 0;
+    r = prepared(dev, {kPrepUmma, kUmmaBf16, 1, pair, int64_t(smem)}, &one, [&](int* v) {
+        const cudaError_t e2 = umma_prepare(kUmmaBf16, true, pair, smem);
+        if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFuncSetAttribute(grouped GEMM)");
+        *v = 1;
+        return int(GBR_OK);
+    });
+    if (r != GBR_OK) return r;
+    cudaError_t e;
     const int grid = pair * int(std::min<int64_t>(s.num_tiles, c->sm_count / pair));
     if ((e = launch_gemm_umma_grouped(pair, mx, mw, mc, g, s, int64_t(N), grid, smem,
                                       reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
