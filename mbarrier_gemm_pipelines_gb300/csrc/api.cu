@@ -43,9 +43,8 @@ struct DevCtx {
 };
 DevCtx g_dev[kMaxDevices];
 
-// Per-device memo of launch preparation (raising a kernel's dynamic shared
-// memory limit, querying its occupancy): done once per (kernel, size), not on
-// every call.  Key: {operator, dtype/kind, grouped, pair, smem bytes}.
+// Per-device memo of occupancy queries (pure functions of kernel and shared
+// memory size).  Key: {operator, dtype/kind, grouped, pair, smem bytes}.
 using PrepKey = std::array<int64_t, 5>;
 std::mutex g_prep_mu;
 std::map<PrepKey, int> g_prep[kMaxDevices];
@@ -67,7 +66,7 @@ int prepared(int dev, const PrepKey& key, int* value, F&& prepare) {
     return GBR_OK;
 }
 
-enum PrepOp : int64_t { kPrepCopy = 1, kPrepFfma = 2, kPrepUmma = 3 };
+enum PrepOp : int64_t { kPrepCopy = 1, kPrepFfma = 2 };
 
 int fail(int code, const char* fmt, ...) {
     char buf[512];
@@ -447,12 +446,11 @@ int staged_copy(const void* src, void* dst, int64_t rows, int64_t cols, int tile
 
     const size_t smem = copy_smem_bytes(stages, tile_bytes);
     int occ = 0;
+    if (cudaError_t e2 = copy_prepare(smem))
+        return cuda_fail(e2, "cudaFuncSetAttribute(staged copy)");
     r = prepared(dev, {kPrepCopy, 0, 0, 0, int64_t(smem)}, &occ, [&](int* v) {
-        cudaError_t e2 = copy_prepare(smem);
-        if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFuncSetAttribute(staged copy)");
-        if ((e2 = copy_occupancy(smem, v)) != cudaSuccess)
-            return cuda_fail(e2, "occupancy(staged copy)");
-        return int(GBR_OK);
+        const cudaError_t e2 = copy_occupancy(smem, v);
+        return e2 == cudaSuccess ? int(GBR_OK) : cuda_fail(e2, "occupancy(staged copy)");
     });
     if (r != GBR_OK) return r;
     cudaError_t e;
@@ -540,11 +538,10 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
         }
         const size_t smem = ffma_smem_bytes(stages);
         int occ = 0;
+        if ((e = ffma_prepare(smem)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(FFMA)");
         r = prepared(dev, {kPrepFfma, 0, 0, 0, int64_t(smem)}, &occ, [&](int* v) {
-            cudaError_t e2 = ffma_prepare(smem);
-            if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFuncSetAttribute(FFMA)");
-            if ((e2 = ffma_occupancy(smem, v)) != cudaSuccess) return cuda_fail(e2, "occupancy(FFMA)");
-            return int(GBR_OK);
+            const cudaError_t e2 = ffma_occupancy(smem, v);
+            return e2 == cudaSuccess ? int(GBR_OK) : cuda_fail(e2, "occupancy(FFMA)");
         });
         if (r != GBR_OK) return r;
         if (occ < 1) return fail(GBR_ERR_SMEM, "FFMA GEMM does not fit on an SM");
@@ -575,14 +572,8 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
         return r;
     if ((r = check_umma_regs(*c, kind, false, pair)) != GBR_OK) return r;
     const size_t smem = umma_smem_bytes(stages, pair, int(s.k_sub));
-    int one = 0;
-    r = prepared(dev, {kPrepUmma, kind, 0, pair, int64_t(smem)}, &one, [&](int* v) {
-        const cudaError_t e2 = umma_prepare(kind, false, pair, smem);
-        if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFuncSetAttribute(tcgen05 GEMM)");
-        *v = 1;
-        return int(GBR_OK);
-    });
-    if (r != GBR_OK) return r;
+    if ((e = umma_prepare(kind, false, pair, smem)) != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute(tcgen05 GEMM)");
     const int grid = pair * int(std::min<int64_t>(s.num_tiles, c->sm_count / pair));
     float* bt = nullptr;  // TF32 only: K-major copy of B, stream-ordered scratch
     if (K > 0) {
@@ -745,15 +736,8 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
     }
     if ((r = check_umma_regs(*c, kUmmaBf16, true, pair)) != GBR_OK) return r;
     const size_t smem = umma_smem_bytes(stages, pair, int(s.k_sub));
-    int one = 0;
-    r = prepared(dev, {kPrepUmma, kUmmaBf16, 1, pair, int64_t(smem)}, &one, [&](int* v) {
-        const cudaError_t e2 = umma_prepare(kUmmaBf16, true, pair, smem);
-        if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFuncSetAttribute(grouped GEMM)");
-        *v = 1;
-        return int(GBR_OK);
-    });
-    if (r != GBR_OK) return r;
-    cudaError_t e;
+    cudaError_t e = umma_prepare(kUmmaBf16, true, pair, smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(grouped GEMM)");
     const int grid = pair * int(std::min<int64_t>(s.num_tiles, c->sm_count / pair));
     if ((e = launch_gemm_umma_grouped(pair, mx, mw, mc, g, s, int64_t(N), grid, smem,
                                       reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)

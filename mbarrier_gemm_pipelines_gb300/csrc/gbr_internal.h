@@ -6,9 +6,24 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "gbr_common.cuh"
 
 namespace gbr {
+
+// Raises (never lowers) a kernel's dynamic shared-memory limit on the current
+// device.  The limit is one value per kernel: lowering it for a small launch
+// would make a later, larger launch of the same kernel fail.  `slot` holds the
+// value set so far on this device; the caller's lock makes check-and-set atomic.
+inline cudaError_t raise_smem_limit(const void* fn, size_t smem, size_t* slot) {
+    if (smem <= *slot) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e == cudaSuccess) *slot = smem;
+    return e;
+}
+constexpr int kMaxDeviceSlots = 64;
 
 // ------------------------------------------------------------ staged copy
 struct CopyArgs {

@@ -188,8 +188,14 @@ size_t ffma_smem_bytes(int stages) {
 }
 
 cudaError_t ffma_prepare(size_t smem) {
-    return cudaFuncSetAttribute(gemm_ffma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                int(smem));
+    static std::mutex mu;
+    static size_t set[kMaxDeviceSlots] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDeviceSlots) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    return raise_smem_limit(reinterpret_cast<const void*>(gemm_ffma_kernel), smem, &set[dev]);
 }
 
 cudaError_t ffma_occupancy(size_t smem, int* blocks_per_sm) {

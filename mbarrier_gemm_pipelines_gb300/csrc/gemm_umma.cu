@@ -560,10 +560,16 @@ size_t umma_smem_bytes(int stages, int pair, int k_sub) {
 size_t umma_smem_bytes(int stages) { return umma_smem_bytes(stages, 1); }
 
 cudaError_t umma_prepare(int kind, bool grouped, int pair, size_t smem) {
+    static std::mutex mu;
+    static size_t set[kMaxDeviceSlots][2][2][2][2] = {};   // [dev][kind][grouped][pair-1][ksub-1]
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDeviceSlots) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
     for (int ksub = 1; ksub <= 2; ++ksub) {
-        const cudaError_t e = cudaFuncSetAttribute(select_kernel(kind, grouped, pair, ksub),
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   int(smem));
+        e = raise_smem_limit(select_kernel(kind, grouped, pair, ksub), smem,
+                             &set[dev][kind][grouped ? 1 : 0][pair - 1][ksub - 1]);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -96,8 +96,14 @@ size_t copy_smem_bytes(int stages, uint32_t tile_bytes) {
 }
 
 cudaError_t copy_prepare(size_t smem) {
-    return cudaFuncSetAttribute(staged_copy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                int(smem));
+    static std::mutex mu;
+    static size_t set[kMaxDeviceSlots] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDeviceSlots) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    return raise_smem_limit(reinterpret_cast<const void*>(staged_copy_kernel), smem, &set[dev]);
 }
 
 cudaError_t copy_occupancy(size_t smem, int* blocks_per_sm) {

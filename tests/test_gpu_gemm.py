@@ -231,3 +231,33 @@ def test_wait_timeout_is_reported_and_context_survives(gbr):
     A, B, bias = inputs.gemm_uniform(128, 256, 64, seed=1)
     got = _run(gbr, A, B, bias, "tf32", 2)
     _check_full(got, A, B, bias, "tf32")
+
+
+def test_launch_order_does_not_matter(gbr):
+    """Deep ring, then shallow ring, then deep ring again on the same kernels:
+    a kernel's shared-memory limit must only ever be raised, never lowered by a
+    smaller launch."""
+    from mbarrier_gemm_pipelines_gb300 import _binding as b
+    A, B, bias = inputs.gemm_normal(384, 512, 640, seed=12)
+    Ab, Bb = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    for dtype, S_list in (("bf16", (6, 1, 6, 3, 1, 3)), ("tf32", (6, 1, 6)), ("ffma", (7, 1, 7))):
+        a, bb = (Ab, Bb) if dtype == "bf16" else (A, B)
+        for S in S_list:
+            got = _run(gbr, a, bb, bias, dtype, S)
+            _check_full(got, a.float(), bb.float(), bias, dtype)
+    src = torch.arange(512 * 64, dtype=torch.float32).reshape(512, 64).cuda()
+    for S in (7, 2, 7):
+        dst = gbr.staged_copy(src, tile=(128, 64), stages=S)
+        gbr.check_device()
+        assert torch.equal(dst, src)
+    # the allocation-free TF32 variant sets limits on the same one-CTA kernels
+    dA, dB, db = A.cuda(), B.cuda(), bias.cuda()
+    C = torch.empty((384, 512), device="cuda")
+    with tuned(gbr, 1):
+        for S in (4, 1):
+            assert b.lib().gemm_bias_relu_tf32_noalloc(
+                dA.data_ptr(), dB.data_ptr(), db.data_ptr(), C.data_ptr(), 384, 512, 640, S,
+                torch.cuda.current_stream().cuda_stream) == b.OK
+            gbr.check_device()
+            got = _run(gbr, A, B, bias, "tf32", 4)
+            _check_full(got, A, B, bias, "tf32")
