@@ -255,7 +255,9 @@ def measure_workloads(gbr, peaks, sm_mhz=None, steps=20, warmup=3):
     from mbarrier_gemm_pipelines_gb300 import inputs
     stream = torch.cuda.current_stream()
     bf16_peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    clock_ghz = (sm_mhz or peaks.get("sm_max_mhz", 2070.0)) / 1e3
+    # The ALU peak at the maximum SM clock: conservative, and independent of the
+    # clock the bf16 run happened to be capped at.
+    clock_ghz = peaks.get("sm_max_mhz", 2070.0) / 1e3
     fp32_alu_peak = 152 * 128 * 2 * clock_ghz / 1e3          # TFLOP/s
     out = {}
 

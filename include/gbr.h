@@ -165,9 +165,11 @@ int gbr_set_wait_timeout_ns(uint64_t ns);
  * Staged-copy tuning, process-wide.  store_lag: -1 auto, 0 (release a slot
  * once its own store has read it) or 1 (release the previous slot after the
  * next store is issued; needs stages >= 2).  ctas_per_sm: -1 auto (as many
- * as shared memory allows), else 1..occupancy.
+ * as shared memory allows), else 1..occupancy.  l2_hint: L2 eviction priority
+ * of the copied lines: -1 auto (1), 0 none, 1 loads evict_first, 2 stores
+ * evict_first, 3 both.
  */
-int gbr_copy_tuning(int store_lag, int ctas_per_sm);
+int gbr_copy_tuning(int store_lag, int ctas_per_sm, int l2_hint);
 
 /*
  * Tensor-core GEMM tuning, process-wide (gemm_bias_relu with GBR_BF16 or

@@ -33,7 +33,7 @@ SIGNATURES = {
     "gbr_launch_count": (ctypes.c_longlong, []),
     "gbr_sm_count": (_i32, []),
     "gbr_set_wait_timeout_ns": (_i32, [_u64]),
-    "gbr_copy_tuning": (_i32, [_i32, _i32]),
+    "gbr_copy_tuning": (_i32, [_i32, _i32, _i32]),
     "gbr_gemm_tuning": (_i32, [_i32, _i32, _i32, _i32]),
     "gbr_selftest_wait_timeout": (_i32, [_u64, _vp]),
     "gemm_bias_relu_tf32_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
@@ -196,8 +196,9 @@ def set_wait_timeout_ns(ns: int) -> None:
     check(lib().gbr_set_wait_timeout_ns(int(ns)))
 
 
-def copy_tuning(store_lag: int = -1, ctas_per_sm: int = -1) -> None:
-    check(lib().gbr_copy_tuning(int(store_lag), int(ctas_per_sm)))
+def copy_tuning(store_lag: int = -1, ctas_per_sm: int = -1, l2_hint: int = -1) -> None:
+    """Staged-copy knobs (see gbr.h): slot-release lag, CTAs per SM, L2 hint."""
+    check(lib().gbr_copy_tuning(int(store_lag), int(ctas_per_sm), int(l2_hint)))
 
 
 def gemm_tuning(cta_pair: int = -1, group_m: int = -1, l2_hint: int = -1,

@@ -36,6 +36,7 @@ struct CopyArgs {
     int32_t store_lag;             // 0: release a slot when its own store has read it
                                    // 1: release the previous slot after issuing the next store
     KernelCtl ctl;
+    uint32_t l2_hint;              // 0 none, 1 loads evict_first, 2 stores evict_first, 3 both
 };
 
 size_t copy_smem_bytes(int stages, uint32_t tile_bytes);

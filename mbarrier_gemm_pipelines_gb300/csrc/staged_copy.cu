@@ -44,6 +44,9 @@ __global__ void __launch_bounds__(64, 1)
     __syncthreads();
 
     const uint32_t ring_base = ptx::smem_addr(ring);
+    // Every byte is read once and written once: optionally tell L2 to evict
+    // these lines first, so they do not push out lines that will be reused.
+    const bool hint_load = (a.l2_hint & 1u) != 0, hint_store = (a.l2_hint & 2u) != 0;
     if (warp == 0 && lane == 0) {
         // ---------------- producer: wait empty -> expect_tx -> TMA load
         uint32_t i = 0;
@@ -55,8 +58,12 @@ __global__ void __launch_bounds__(64, 1)
             const uint32_t fb = ptx::smem_addr(full + s);
             ptx::mbar_arrive_expect_tx(fb, a.tile_bytes);
             const int32_t tr = int32_t(t / a.tiles_c), tc = int32_t(t % a.tiles_c);
-            ptx::tma_load_2d(ring_base + s * a.tile_bytes, &src_map, fb, tc * a.tile_cols,
-                             tr * a.tile_rows);
+            if (hint_load)
+                ptx::tma_load_2d_hint(ring_base + s * a.tile_bytes, &src_map, fb, tc * a.tile_cols,
+                                      tr * a.tile_rows, ptx::l2_policy_evict_first());
+            else
+                ptx::tma_load_2d(ring_base + s * a.tile_bytes, &src_map, fb, tc * a.tile_cols,
+                                 tr * a.tile_rows);
         }
         if (*abort_flag) {
             // Let this CTA's own loads in flight land before the CTA exits.
@@ -72,8 +79,12 @@ __global__ void __launch_bounds__(64, 1)
             if (!mbar_wait(ptx::smem_addr(full + s), ph, a.ctl, abort_flag, kSiteStorerFull, i))
                 break;
             const int32_t tr = int32_t(t / a.tiles_c), tc = int32_t(t % a.tiles_c);
-            ptx::tma_store_2d(&dst_map, ring_base + s * a.tile_bytes, tc * a.tile_cols,
-                              tr * a.tile_rows);
+            if (hint_store)
+                ptx::tma_store_2d_hint(&dst_map, ring_base + s * a.tile_bytes, tc * a.tile_cols,
+                                       tr * a.tile_rows, ptx::l2_policy_evict_first());
+            else
+                ptx::tma_store_2d(&dst_map, ring_base + s * a.tile_bytes, tc * a.tile_cols,
+                                  tr * a.tile_rows);
             ptx::bulk_commit_group();
             if (a.store_lag == 0) {
                 ptx::bulk_wait_group_read<0>();

@@ -55,18 +55,18 @@ def test_copy_special_values(gbr):
 
 
 @pytest.mark.parametrize("S", [2, 4, 7])
-@pytest.mark.parametrize("store_lag", [-1, 0])
-def test_copy_full_size_bit_exact(gbr, S, store_lag):
+@pytest.mark.parametrize("store_lag,l2_hint", [(-1, -1), (0, -1), (-1, 3), (1, 1)])
+def test_copy_full_size_bit_exact(gbr, S, store_lag, l2_hint):
     src = inputs.workload("copy")
     expect = oracle.copy(src.numpy())
     d_src = src.cuda()
     dst = torch.empty_like(d_src)
-    gbr.copy_tuning(store_lag, -1)
+    gbr.copy_tuning(store_lag, -1, l2_hint)
     try:
         gbr.staged_copy(d_src, dst, tile=(128, 64), stages=S)
         gbr.check_device()
     finally:
-        gbr.copy_tuning(-1, -1)
+        gbr.copy_tuning(-1, -1, -1)
     assert np.array_equal(_bits(dst), expect.view(np.int32))
 
 
