@@ -283,6 +283,20 @@ def measure_workloads(gbr, peaks, sm_mhz=None, steps=20, warmup=3):
                 "value": round(v, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
                 "roofline": {"bound": bound, "achieved": round(v, 2), "peak": round(peak, 1),
                              "unit": "TFLOP/s", "frac": round(v / peak, 4), "peak_note": unit}}
+    # The pages' central comparison on GB300: the homogeneous load/sync/compute/
+    # sync loop versus the warp-specialized ring at depths 1-4 (same tile, same
+    # FFMA micro-kernel).
+    v, ms = timed(lambda: gbr.gemm_bias_relu(dA, dB, db, dC, dtype="ffma_sync", stages=1), f)
+    out["gemm_fp32_4096_ffma_homogeneous"] = {
+        "value": round(v, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
+        "roofline": {"bound": "alu", "achieved": round(v, 2), "peak": round(fp32_alu_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(v / fp32_alu_peak, 4)}}
+    for S in (1, 2):
+        v, ms = timed(lambda: gbr.gemm_bias_relu(dA, dB, db, dC, dtype="ffma", stages=S), f)
+        out["gemm_fp32_4096_ffma_S%d" % S] = {
+            "value": round(v, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
+            "roofline": {"bound": "alu", "achieved": round(v, 2), "peak": round(fp32_alu_peak, 1),
+                         "unit": "TFLOP/s", "frac": round(v / fp32_alu_peak, 4)}}
     del dA, dB, db, dC
     A, B, bias = inputs.workload("gemm_small")
     dA, dB, db = A.cuda(), B.cuda(), bias.cuda()
@@ -302,6 +316,34 @@ def measure_workloads(gbr, peaks, sm_mhz=None, steps=20, warmup=3):
         "roofline": {"bound": "tensor", "achieved": round(v, 2), "peak": bf16_peak,
                      "unit": "TFLOP/s", "frac": round(v / bf16_peak, 4)}}
     return out
+
+
+def run_ablation(args):
+    """Ring depth on the tensor-core GEMM (bf16 8192^3): one CTA or a CTA pair per
+    tile, one or two 128-byte K slices per stage, every depth that fits.  Prints one
+    JSON line of TFLOP/s per variant."""
+    import torch
+    import mbarrier_gemm_pipelines_gb300 as gbr
+    from mbarrier_gemm_pipelines_gb300 import inputs
+    gbr.build()
+    torch.cuda.set_device(0)
+    A, B, bias = inputs.workload("gemm_bf16")
+    dA, dB, db = A.cuda(), B.cuda(), bias.cuda()
+    dC = torch.empty((8192, 8192), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    f = gemm_flops(8192, 8192, 8192)
+    res = {}
+    for pair, ks, depths in ((1, 1, (1, 2, 3, 4)), (2, 1, (1, 2, 3, 4, 5, 6)), (2, 2, (1, 2, 3))):
+        for S in depths:
+            gbr.gemm_tuning(pair, -1, -1, ks)
+            fn = lambda: gbr.gemm_bias_relu(dA, dB, db, dC, dtype="bf16", stages=S)
+            for _ in range(3):
+                fn()
+            t = time_launches(fn, args.steps, stream)
+            gbr.check_device()
+            res["pair%d_kslices%d_S%d" % (pair, ks, S)] = round(f * args.steps / t / 1e12, 1)
+    gbr.gemm_tuning(-1, -1, -1, -1)
+    emit({"ablation": "tensor-core ring depth, bf16 8192^3", "unit": "TFLOP/s", "results": res})
 
 
 def run_ours(args):
@@ -483,13 +525,13 @@ def run_profile_case(case, launches=2, stages=4, pair=-1):
         src = inputs.workload("copy").cuda()
         dst = torch.empty_like(src)
         fn = lambda: gbr.staged_copy(src, dst, tile=(128, 64), stages=stages)
-    elif case in ("gemm_bf16", "gemm_tf32", "gemm_ffma"):
+    elif case in ("gemm_bf16", "gemm_tf32", "gemm_ffma", "gemm_ffma_sync"):
         if case == "gemm_bf16":
             A, B, bias = inputs.workload("gemm_bf16")
         else:
             A, B, bias = inputs.workload("gemm_fp32")
         dA, dB, db = A.cuda(), B.cuda(), bias.cuda()
-        dt = case.split("_")[1]
+        dt = case[len("gemm_"):]
         fn = lambda: gbr.gemm_bias_relu(dA, dB, db, dtype=dt, stages=stages)
     elif case == "grouped":
         counts, X, W, b = inputs.workload("grouped_bf16")
@@ -516,14 +558,19 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="skip the secondary workloads (fp32 4096^3, 256^3, grouped MoE)")
+    ap.add_argument("--ablation", action="store_true",
+                    help="ring-depth sweep of the tensor-core GEMM (one JSON line)")
     ap.add_argument("--dist-selftest", action="store_true",
                     help="check the multi-rank aggregation on CPU (gloo), no GPU work")
     ap.add_argument("--profile", metavar="CASE",
                     help="run two launches of one kernel for ncu: copy, gemm_bf16, gemm_tf32, "
-                         "gemm_ffma or grouped")
+                         "gemm_ffma, gemm_ffma_sync or grouped")
     args = ap.parse_args()
     if args.dist_selftest:
         run_dist_selftest()
+        return
+    if args.ablation:
+        run_ablation(args)
         return
     if args.profile:
         run_profile_case(args.profile, stages=args.stages, pair=args.pair)

@@ -42,9 +42,14 @@ extern "C" {
 typedef struct CUstream_st *gbr_stream_t;
 
 typedef enum {
-    GBR_F32_FFMA = 0, /* fp32 in/out, strict fp32 FMA on CUDA cores        */
-    GBR_F32_TF32 = 1, /* fp32 in/out, TF32 tensor-core multiply, fp32 acc   */
-    GBR_BF16 = 2      /* bf16 A/B/C, fp32 bias, fp32 accumulation in TMEM   */
+    GBR_F32_FFMA = 0,     /* fp32 in/out, strict fp32 FMA on CUDA cores        */
+    GBR_F32_TF32 = 1,     /* fp32 in/out, TF32 tensor-core multiply, fp32 acc   */
+    GBR_BF16 = 2,         /* bf16 A/B/C, fp32 bias, fp32 accumulation in TMEM   */
+    GBR_F32_FFMA_SYNC = 3 /* GBR_F32_FFMA computed by the homogeneous loop of
+                             "pwwt.cn news/4436243" section 1.1 (all threads
+                             load, sync, compute, sync; no roles, no ring):
+                             the baseline the pipeline is measured against.
+                             stages must be 1.                                 */
 } gbr_dtype;
 
 typedef enum {
@@ -66,6 +71,7 @@ typedef enum {
  * "gpu_warp_specialization" ("End-to-end flow").
  *
  *   A     [M, K] row-major; fp32 (GBR_F32_*) or bf16 (GBR_BF16).  Read only.
+ *         (GBR_F32_FFMA_SYNC reads A and B with plain loads, not TMA.)
  *   B     [K, N] row-major; same type as A.  Read only.
  *   bias  [N] fp32.  Read only.
  *   C     [M, N] row-major; fp32 (GBR_F32_*) or bf16 (GBR_BF16, rounded to

@@ -219,6 +219,7 @@ int choose_k_sub(int pair, int stages, int smem_optin) {
 
 // Largest ring depth for the dtype (tcgen05: that of the CTA-pair kernel).
 int gemm_max_stages(int dtype, int smem_optin) {
+    if (dtype == GBR_F32_FFMA_SYNC) return 1;   // single-buffered by definition
     return dtype == GBR_F32_FFMA ? max_stages_for(ffma_bytes_fn, smem_optin)
                                  : umma_max_stages(2, smem_optin);
 }
@@ -343,7 +344,8 @@ int gbr_max_stages(int op, int dtype, int tile_rows, int tile_cols) {
     int r = get_ctx(&c);
     if (r != GBR_OK) return -r;
     if (op == GBR_OP_GEMM) {
-        if (dtype < GBR_F32_FFMA || dtype > GBR_BF16) return -fail(GBR_ERR_INVALID, "bad dtype %d", dtype);
+        if (dtype < GBR_F32_FFMA || dtype > GBR_F32_FFMA_SYNC)
+            return -fail(GBR_ERR_INVALID, "bad dtype %d", dtype);
         return gemm_max_stages(dtype, c->smem_optin);
     }
     if (op == GBR_OP_COPY) {
@@ -473,7 +475,7 @@ int staged_copy(const void* src, void* dst, int64_t rows, int64_t cols, int tile
 
 int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int64_t M, int64_t N,
                    int64_t K, int dtype, int stages, gbr_stream_t stream) {
-    if (dtype < GBR_F32_FFMA || dtype > GBR_BF16)
+    if (dtype < GBR_F32_FFMA || dtype > GBR_F32_FFMA_SYNC)
         return fail(GBR_ERR_INVALID, "gemm_bias_relu: unknown dtype %d", dtype);
     const int64_t lim = int64_t(1) << 31;
     if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim)
@@ -513,6 +515,19 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
     s.ctl = make_ctl(*c);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
+
+    if (dtype == GBR_F32_FFMA_SYNC) {
+        s.m_tiles = int32_t(cdiv(M, kFfmaBM));
+        s.n_tiles = int32_t(cdiv(N, kFfmaBN));
+        s.num_kb = int32_t(cdiv(K, kFfmaBK));
+        s.num_tiles = s.m_tiles * s.n_tiles;
+        s.group_m = 8;
+        if ((e = launch_gemm_ffma_sync(static_cast<const float*>(A), static_cast<const float*>(B), s,
+                                       st)) != cudaSuccess)
+            return cuda_fail(e, "launching the homogeneous FFMA GEMM");
+        ++g_launches;
+        return GBR_OK;
+    }
 
     if (dtype == GBR_F32_FFMA) {
         s.m_tiles = int32_t(cdiv(M, kFfmaBM));

@@ -70,6 +70,10 @@ cudaError_t ffma_occupancy(size_t smem, int* blocks_per_sm);
 cudaError_t ffma_check_registers(int* regs);
 cudaError_t launch_gemm_ffma(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmShape& s,
                              int grid, size_t smem, cudaStream_t stream);
+// Homogeneous baseline (every thread loads, syncs, computes, syncs); one CTA
+// per 128x128 tile, single-buffered, plain global loads.
+cudaError_t launch_gemm_ffma_sync(const float* A, const float* B, const GemmShape& s,
+                                  cudaStream_t stream);
 
 // tcgen05 path: 128x256 output tiles, 128-byte K slices per stage.
 constexpr int kUmmaBM = 128, kUmmaBN = 256;

@@ -30,6 +30,69 @@ constexpr uint32_t kBPanelBytes = kFfmaBK * 128;      // 32 rows x 128 B
 constexpr uint32_t kProducerRegs = 40;
 constexpr uint32_t kConsumerRegs = 232;
 
+// One 32-deep K stage of the 128 x 128 tile for thread (tx, ty): rows
+// ty + 16 r, columns 4 tx .. 4 tx + 3 and 64 + 4 tx .. 64 + 4 tx + 3.  All of
+// the thread's rows share one swizzle phase per k-group and all its columns
+// one phase per k, read from the tables a_sw / b_sw, so every shared-memory
+// load is base + immediate offset.
+__device__ __forceinline__ void ffma_stage(float (&acc)[8][8], const uint8_t* As, const uint8_t* Bs,
+                                           const uint32_t (&a_sw)[8], const uint32_t (&b_sw)[8]) {
+#pragma unroll
+    for (uint32_t k4 = 0; k4 < kFfmaBK / 4; ++k4) {
+        const uint8_t* ap = As + a_sw[k4];
+        float4 a[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) a[r] = *reinterpret_cast<const float4*>(ap + r * 16 * 128);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t k = 4 * k4 + kk;
+            const uint8_t* bp = Bs + b_sw[k & 7u] + k * 128u;
+            const float4 b0 = *reinterpret_cast<const float4*>(bp);
+            const float4 b1 = *reinterpret_cast<const float4*>(bp + 2 * kBPanelBytes);
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const float av = kk == 0 ? a[r].x : kk == 1 ? a[r].y : kk == 2 ? a[r].z : a[r].w;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av, bv[c], acc[r][c]);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void ffma_tables(uint32_t tx, uint32_t ty, uint32_t (&a_sw)[8],
+                                            uint32_t (&b_sw)[8]) {
+#pragma unroll
+    for (uint32_t j = 0; j < 8; ++j) {
+        a_sw[j] = ty * 128u + ((j ^ (ty & 7u)) << 4);                 // row ty, chunk j
+        b_sw[j] = (tx >> 3) * kBPanelBytes + (((tx & 7u) ^ j) << 4);  // column 4 tx, K row % 8 = j
+    }
+}
+
+// C = max(0, acc + bias) for the thread's 8 x 8 outputs of tile (mt, nt).
+__device__ __forceinline__ void ffma_epilogue(const float (&acc)[8][8], const GemmShape& p,
+                                              uint32_t mt, uint32_t nt, uint32_t tx, uint32_t ty) {
+    float* C = static_cast<float*>(p.C);
+    const int n0 = int(nt) * kFfmaBN, m0 = int(mt) * kFfmaBM;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int n = n0 + int(4 * tx) + 64 * h;
+        if (n >= p.N) continue;
+        const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + n));
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int m = m0 + int(ty) + 16 * r;
+            if (m >= p.M) continue;
+            float4 v;
+            v.x = fmaxf(acc[r][4 * h + 0] + bb.x, 0.f);
+            v.y = fmaxf(acc[r][4 * h + 1] + bb.y, 0.f);
+            v.z = fmaxf(acc[r][4 * h + 2] + bb.z, 0.f);
+            v.w = fmaxf(acc[r][4 * h + 3] + bb.w, 0.f);
+            *reinterpret_cast<float4*>(C + size_t(m) * p.N + n) = v;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_ffma_kernel(const __grid_constant__ CUtensorMap mapA,
                      const __grid_constant__ CUtensorMap mapB, const GemmShape p) {
@@ -101,11 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ct = threadIdx.x - 128;        // 0..255
         const uint32_t tx = ct & 15u, ty = ct >> 4;
         uint32_t a_sw[8], b_sw[8];
-#pragma unroll
-        for (uint32_t j = 0; j < 8; ++j) {
-            a_sw[j] = ty * 128u + ((j ^ (ty & 7u)) << 4);                 // row ty, chunk j
-            b_sw[j] = (tx >> 3) * kBPanelBytes + (((tx & 7u) ^ j) << 4);  // column 4 tx, K row % 8 = j
-        }
+        ffma_tables(tx, ty, a_sw, b_sw);
 
         uint32_t i = 0;
         bool ok = true;
@@ -126,62 +185,84 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint8_t* As = ring + size_t(s) * kFfmaStageBytes;
-                const uint8_t* Bs = As + kABytes;
-#pragma unroll
-                for (uint32_t k4 = 0; k4 < kFfmaBK / 4; ++k4) {
-                    const uint8_t* ap = As + a_sw[k4];
-                    float4 a[8];
-#pragma unroll
-                    for (int r = 0; r < 8; ++r)
-                        a[r] = *reinterpret_cast<const float4*>(ap + r * 16 * 128);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t k = 4 * k4 + kk;
-                        const uint8_t* bp = Bs + b_sw[k & 7u] + k * 128u;
-                        const float4 b0 = *reinterpret_cast<const float4*>(bp);
-                        const float4 b1 = *reinterpret_cast<const float4*>(bp + 2 * kBPanelBytes);
-                        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-                        for (int r = 0; r < 8; ++r) {
-                            const float av = kk == 0 ? a[r].x : kk == 1 ? a[r].y
-                                           : kk == 2 ? a[r].z : a[r].w;
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av, bv[c], acc[r][c]);
-                        }
-                    }
-                }
+                ffma_stage(acc, As, As + kABytes, a_sw, b_sw);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(empty + s));
             }
             if (!ok) break;
 
-            // ------------------------------------------------ epilogue
-            float* C = static_cast<float*>(p.C);
-            const int n0 = int(nt) * kFfmaBN, m0 = int(mt) * kFfmaBM;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int n = n0 + int(4 * tx) + 64 * h;
-                if (n >= p.N) continue;
-                const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + n));
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int m = m0 + int(ty) + 16 * r;
-                    if (m >= p.M) continue;
-                    float4 v;
-                    v.x = fmaxf(acc[r][4 * h + 0] + bb.x, 0.f);
-                    v.y = fmaxf(acc[r][4 * h + 1] + bb.y, 0.f);
-                    v.z = fmaxf(acc[r][4 * h + 2] + bb.z, 0.f);
-                    v.w = fmaxf(acc[r][4 * h + 3] + bb.w, 0.f);
-                    *reinterpret_cast<float4*>(C + size_t(m) * p.N + n) = v;
-                }
-            }
+            ffma_epilogue(acc, p, mt, nt, tx, ty);
         }
     }
     __syncwarp();
     __syncthreads();
 }
 
+// The homogeneous baseline of "pwwt.cn news/4436243", section 1.1: every
+// thread loads its share of the next K tile from global memory into shared
+// memory, the block synchronises, every thread computes on the tile, and the
+// block synchronises again before the buffer may be overwritten.  Same tile,
+// same shared-memory layout and same FFMA micro-kernel as the warp-specialized
+// kernel above; no roles, no ring, no mbarriers.  One CTA per output tile.
+constexpr int kSyncThreads = 256;
+
+__global__ void __launch_bounds__(kSyncThreads, 2) gemm_ffma_sync_kernel(const float* __restrict__ A,
+                                                                         const float* __restrict__ B,
+                                                                         const GemmShape p) {
+    __shared__ __align__(1024) uint8_t tile[kFfmaStageBytes];
+    uint8_t* As = tile;
+    uint8_t* Bs = tile + kABytes;
+    const uint32_t t = threadIdx.x;
+    const uint32_t tx = t & 15u, ty = t >> 4;
+    uint32_t mt, nt;
+    raster_tile(blockIdx.x, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+    const int m0 = int(mt) * kFfmaBM, n0 = int(nt) * kFfmaBN;
+    uint32_t a_sw[8], b_sw[8];
+    ffma_tables(tx, ty, a_sw, b_sw);
+    float acc[8][8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+
+    for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int k0 = kb * kFfmaBK;
+        // load: 4 float4 of A (row idx/8, 16-byte chunk idx%8) and 4 of B
+        // (K row idx/32, 16-byte chunk idx%32) per thread, zero outside the
+        // matrix, stored in the same swizzled layout the TMA path produces.
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t idx = t + kSyncThreads * j;
+            const uint32_t row = idx >> 3, k4 = idx & 7u;
+            const int m = m0 + int(row), k = k0 + int(4 * k4);
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (m < p.M && k < p.K) v = __ldg(reinterpret_cast<const float4*>(A + size_t(m) * p.K + k));
+            *reinterpret_cast<float4*>(As + row * 128u + ((k4 ^ (row & 7u)) << 4)) = v;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t idx = t + kSyncThreads * j;
+            const uint32_t kr = idx >> 5, n4 = idx & 31u;
+            const int k = k0 + int(kr), n = n0 + int(4 * n4);
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k < p.K && n < p.N) v = __ldg(reinterpret_cast<const float4*>(B + size_t(k) * p.N + n));
+            *reinterpret_cast<float4*>(Bs + (n4 >> 3) * kBPanelBytes + kr * 128u +
+                                       (((n4 & 7u) ^ (kr & 7u)) << 4)) = v;
+        }
+        __syncthreads();   // the whole tile has arrived
+        ffma_stage(acc, As, Bs, a_sw, b_sw);
+        __syncthreads();   // every thread is done with it
+    }
+    ffma_epilogue(acc, p, mt, nt, tx, ty);
+}
+
 }  // namespace
+
+cudaError_t launch_gemm_ffma_sync(const float* A, const float* B, const GemmShape& s,
+                                  cudaStream_t stream) {
+    gemm_ffma_sync_kernel<<<s.num_tiles, kSyncThreads, 0, stream>>>(A, B, s);
+    return cudaGetLastError();
+}
 
 size_t ffma_smem_bytes(int stages) {
     return 1024 + size_t(stages) * kFfmaStageBytes + size_t(2 * stages) * 8 + 16;

@@ -261,3 +261,27 @@ def test_launch_order_does_not_matter(gbr):
             gbr.check_device()
             got = _run(gbr, A, B, bias, "tf32", 4)
             _check_full(got, A, B, bias, "tf32")
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_homogeneous_baseline_small(gbr, M, N, K):
+    """The section 1.1 loop (all threads load, sync, compute, sync) computes the
+    same C as the pipeline, to the FFMA bar."""
+    A, B, bias = inputs.gemm_uniform(M, N, K, seed=M * 17 + N * 3 + K)
+    got = _run(gbr, A, B, bias, "ffma_sync", 1)
+    _check_full(got, A, B, bias, "ffma")
+
+
+def test_homogeneous_baseline_4096_and_limits(gbr):
+    A, B, bias = inputs.workload("gemm_fp32")
+    _sampled(gbr, A, B, bias, "ffma_sync", 1, 2000, seed=2)
+    assert gbr.max_stages(gbr.OP_GEMM, 3) == 1
+    with pytest.raises(gbr.GbrError) as e:
+        gbr.gemm_bias_relu(A[:64, :64].contiguous().cuda(), B[:64, :64].contiguous().cuda(),
+                           bias[:64].contiguous().cuda(), dtype="ffma_sync", stages=2)
+    assert e.value.code == 4
+    bias_only = torch.linspace(-1, 1, 136)
+    C = gbr.gemm_bias_relu(torch.empty((50, 0)).cuda(), torch.empty((0, 136)).cuda(),
+                           bias_only.cuda(), dtype="ffma_sync", stages=1)
+    gbr.check_device()
+    assert torch.equal(C.cpu(), torch.clamp(bias_only, min=0).expand(50, 136))
