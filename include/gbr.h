@@ -202,6 +202,35 @@ int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage);
 int gbr_selftest_wait_timeout(uint64_t timeout_ns, gbr_stream_t stream);
 
 /*
+ * Failure-detection self tests of the real pipelines.  Each runs the normal
+ * call once with one fault planted on the host's instructions: in CTA `cta`,
+ * ring item `item` (that CTA's item counter, counted from 0 across its tiles),
+ * the producer registers the stage's expected bytes on the full barrier but
+ * issues no TMA load, so that stage never fills.  The consumer's bounded wait
+ * (limit `limit_ns`, in (0, 10 s]) gives up, records the site, raises the
+ * CTA's abort flag; the other roles leave their loops, the producer waits
+ * for its own loads in flight, the tensor-core kernel waits for its issued
+ * MMAs and frees its Tensor Memory, and the kernel returns.  Other CTAs run
+ * normally.  gbr_device_status() then reports GBR_ERR_TIMEOUT with the site
+ * (0x21 FFMA consumer, 0x31 MMA issuer or 0x41 epilogue, 0x51 copy storer),
+ * the CTA and the item; the output is undefined.  If `cta` or `item` does not
+ * exist in that launch nothing is planted and the call completes normally.
+ *
+ * gbr_selftest_gemm_skip_load: arguments as gemm_bias_relu; dtype GBR_F32_FFMA,
+ *   GBR_F32_TF32 or GBR_BF16 (the tensor-core dtypes run one CTA per tile, so
+ *   `stages` must fit that kernel).
+ * gbr_selftest_copy_skip_load: arguments as staged_copy with 128 x 64 tiles.
+ * Returns GBR_OK when launched, GBR_ERR_INVALID for a negative cta or item or
+ * a limit out of range, and the errors of the wrapped call.
+ */
+int gbr_selftest_gemm_skip_load(const void *A, const void *B, const float *bias, void *C,
+                                int64_t M, int64_t N, int64_t K, int dtype, int stages, int cta,
+                                int item, uint64_t limit_ns, gbr_stream_t stream);
+int gbr_selftest_copy_skip_load(const void *src, void *dst, int64_t rows, int64_t cols,
+                                int stages, int cta, int item, uint64_t limit_ns,
+                                gbr_stream_t stream);
+
+/*
  * gemm_bias_relu_tf32_noalloc -- the GBR_F32_TF32 case of gemm_bias_relu for
  * callers that cannot allocate device memory.  It has no counterpart in the
  * pages; it exists for code that may not call cudaMalloc or cudaMallocAsync:

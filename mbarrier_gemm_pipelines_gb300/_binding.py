@@ -36,6 +36,9 @@ SIGNATURES = {
     "gbr_copy_tuning": (_i32, [_i32, _i32, _i32]),
     "gbr_gemm_tuning": (_i32, [_i32, _i32, _i32, _i32]),
     "gbr_selftest_wait_timeout": (_i32, [_u64, _vp]),
+    "gbr_selftest_gemm_skip_load": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32,
+                                           _i32, _u64, _vp]),
+    "gbr_selftest_copy_skip_load": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _i32, _u64, _vp]),
     "gemm_bias_relu_tf32_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
 }
 
@@ -211,6 +214,37 @@ def gemm_tuning(cta_pair: int = -1, group_m: int = -1, l2_hint: int = -1,
 
 def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
     check(lib().gbr_selftest_wait_timeout(int(timeout_ns), _stream_ptr(stream)))
+
+
+def selftest_gemm_skip_load(A, B, bias, dtype, stages, cta, item, limit_ns, stream=None):
+    """Runs gemm_bias_relu with one stage of CTA `cta`, ring item `item`, left
+    unfilled (see gbr.h); returns the (undefined) output tensor."""
+    import torch
+    code = DTYPE_NAMES[dtype] if isinstance(dtype, str) else int(dtype)
+    want = (torch.bfloat16,) if code == BF16 else (torch.float32,)
+    _cuda_tensor(A, "A", want)
+    _cuda_tensor(B, "B", want)
+    _cuda_tensor(bias, "bias", (torch.float32,))
+    M, K = A.shape
+    N = B.shape[1]
+    C = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    check(lib().gbr_selftest_gemm_skip_load(A.data_ptr(), B.data_ptr(), bias.data_ptr(),
+                                            C.data_ptr(), M, N, K, code, int(stages), int(cta),
+                                            int(item), int(limit_ns), _stream_ptr(stream)))
+    return C
+
+
+def selftest_copy_skip_load(src, stages, cta, item, limit_ns, stream=None):
+    """Runs staged_copy (128 x 64 tiles) with one stage of CTA `cta`, ring item
+    `item`, left unfilled (see gbr.h); returns the (undefined) output tensor."""
+    import torch
+    _cuda_tensor(src, "src", (torch.float32,))
+    dst = torch.empty_like(src)
+    rows, cols = src.shape
+    check(lib().gbr_selftest_copy_skip_load(src.data_ptr(), dst.data_ptr(), rows, cols,
+                                            int(stages), int(cta), int(item), int(limit_ns),
+                                            _stream_ptr(stream)))
+    return dst
 
 
 def gemm_bias_relu_tf32_noalloc(A, B, bias, C, stages=4, stream=None):

@@ -20,6 +20,10 @@ namespace gbr {
 namespace {
 
 thread_local std::string t_last_error;
+// Failure-detection self test: injection and wait limit for the next launch on
+// this thread (set and cleared by the gbr_selftest_* entry points only).
+thread_local FaultInjection t_inject = {0, 0, 0};
+thread_local uint64_t t_timeout_override = 0;
 std::atomic<long long> g_launches{0};
 std::mutex g_mu;
 uint64_t g_timeout_ns = 0;  // 0: not yet resolved
@@ -125,8 +129,22 @@ int get_ctx(DevCtx** out, int* dev_out = nullptr) {
 KernelCtl make_ctl(const DevCtx& c) {
     KernelCtl k;
     k.status = c.status;
-    k.timeout_ns = timeout_ns();
+    k.timeout_ns = t_timeout_override ? t_timeout_override : timeout_ns();
     return k;
+}
+
+// Runs `call` with a fault injected into the next pipeline launch of this thread.
+template <class F>
+int with_injection(int cta, int item, uint64_t limit_ns, F&& call) {
+    if (cta < 0 || item < 0) return fail(GBR_ERR_INVALID, "self test: cta and item must be >= 0");
+    if (limit_ns == 0 || limit_ns > 10000000000ull)
+        return fail(GBR_ERR_INVALID, "self test: limit must be in (0, 10 s]");
+    t_inject = FaultInjection{1u, cta, item};
+    t_timeout_override = limit_ns;
+    const int r = call();
+    t_inject = FaultInjection{0u, 0, 0};
+    t_timeout_override = 0;
+    return r;
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -383,6 +401,23 @@ int gbr_device_status(gbr_stream_t stream) {
                 st[1], st[2], st[3]);
 }
 
+int gbr_selftest_gemm_skip_load(const void* A, const void* B, const float* bias, void* C,
+                                int64_t M, int64_t N, int64_t K, int dtype, int stages, int cta,
+                                int item, uint64_t limit_ns, gbr_stream_t stream) {
+    if (dtype == GBR_F32_FFMA_SYNC)
+        return fail(GBR_ERR_UNSUPPORTED, "self test: the homogeneous loop has no ring to break");
+    return with_injection(cta, item, limit_ns, [&] {
+        return gemm_bias_relu(A, B, bias, C, M, N, K, dtype, stages, stream);
+    });
+}
+
+int gbr_selftest_copy_skip_load(const void* src, void* dst, int64_t rows, int64_t cols, int stages,
+                                int cta, int item, uint64_t limit_ns, gbr_stream_t stream) {
+    return with_injection(cta, item, limit_ns, [&] {
+        return staged_copy(src, dst, rows, cols, 128, 64, stages, stream);
+    });
+}
+
 int gbr_selftest_wait_timeout(uint64_t timeout_ns_limit, gbr_stream_t stream) {
     DevCtx* c;
     int r = get_ctx(&c);
@@ -450,6 +485,7 @@ int staged_copy(const void* src, void* dst, int64_t rows, int64_t cols, int tile
     // Auto: the loaded lines are marked evict-first (each is read exactly once);
     // measured on the 256 MiB copy, +4% over no hint.
     a.l2_hint = hint < 0 ? 1u : uint32_t(hint);
+    a.inject = t_inject;
     a.store_lag = (lag < 0) ? (stages >= 2 ? 1 : 0) : lag;
     if (a.store_lag == 1 && stages < 2) a.store_lag = 0;
     a.ctl = make_ctl(*c);
@@ -513,6 +549,7 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
     s.bias = bias;
     s.C = C;
     s.ctl = make_ctl(*c);
+    s.inject = t_inject;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
 
@@ -582,7 +619,14 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
     const uint32_t panel_cols = uint32_t(128 / es);  // B panel width; also the C store box width
     int pair = 1;
     if ((r = choose_pair(M, stages, c->smem_optin, &pair)) != GBR_OK) return r;
-    s.k_sub = uint32_t(choose_k_sub(pair, stages, c->smem_optin));
+    if (s.inject.enabled) {
+        // The self test runs one CTA per tile: there the abort path drains
+        // exactly the loads its own producer issued.
+        if (stages > umma_max_stages(1, c->smem_optin))
+            return fail(GBR_ERR_SMEM, "self test: stages must fit one CTA per tile");
+        pair = 1;
+    }
+    s.k_sub = uint32_t(s.inject.enabled ? 1 : choose_k_sub(pair, stages, c->smem_optin));
     s.m_tiles = int32_t(cdiv(M, int64_t(kUmmaBM) * pair));
     s.n_tiles = int32_t(cdiv(N, kUmmaBN));
     s.num_kb = int32_t(cdiv(K, int64_t(bk) * s.k_sub));

@@ -25,6 +25,19 @@ inline cudaError_t raise_smem_limit(const void* fn, size_t smem, size_t* slot) {
 }
 constexpr int kMaxDeviceSlots = 64;
 
+// Failure-detection self test: the producer of CTA `cta` registers the bytes
+// of its ring item `item` with expect_tx but issues no TMA load for it, so the
+// consumer's bounded wait on that stage must run out.  All zero: no injection.
+struct FaultInjection {
+    uint32_t enabled;
+    int32_t cta;
+    int32_t item;
+};
+
+__device__ __forceinline__ bool inject_skip(const FaultInjection& f, uint32_t item) {
+    return f.enabled != 0 && int32_t(blockIdx.x) == f.cta && int32_t(item) == f.item;
+}
+
 // ------------------------------------------------------------ staged copy
 struct CopyArgs {
     int32_t rows, cols;            // fp32 elements
@@ -37,6 +50,7 @@ struct CopyArgs {
                                    // 1: release the previous slot after issuing the next store
     KernelCtl ctl;
     uint32_t l2_hint;              // 0 none, 1 loads evict_first, 2 stores evict_first, 3 both
+    FaultInjection inject;         // failure-detection self test only (zeroed: none)
 };
 
 size_t copy_smem_bytes(int stages, uint32_t tile_bytes);
@@ -59,6 +73,7 @@ struct GemmShape {
     uint32_t l2_hint;              // tensor-core GEMM operand loads: 0 none, 1 A and B
                                    // evict_last, 2 A evict_first / B evict_last,
                                    // 3 A evict_last / B evict_first, 4 both evict_normal
+    FaultInjection inject;         // failure-detection self test only (zeroed: none)
 };
 
 // FFMA path (strict fp32, CUDA cores): 128x128x32 tiles.

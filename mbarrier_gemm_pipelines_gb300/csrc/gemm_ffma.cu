@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t fb = ptx::smem_addr(full + s);
                     ptx::mbar_arrive_expect_tx(fb, kFfmaStageBytes);
+                    if (inject_skip(p.inject, i)) continue;   // self test: stage never fills
                     const uint32_t st = ring_base + s * kFfmaStageBytes;
                     ptx::tma_load_2d(st, &mapA, fb, kb * kFfmaBK, int(mt) * kFfmaBM);
 #pragma unroll

@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb_local = ptx::smem_addr(full + slot);
                     const uint32_t fb = PAIR == 2 ? ptx::mapa_shared(fb_local, 0) : fb_local;
                     if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, PAIR * stage_bytes);
+                    if (PAIR == 1 && inject_skip(s.inject, it)) continue;   // self test
                     const uint32_t stage_base = ring_base + slot * stage_bytes;
 #pragma unroll
                     for (uint32_t h = 0; h < ksub; ++h) {

@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(64, 1)
                 break;
             const uint32_t fb = ptx::smem_addr(full + s);
             ptx::mbar_arrive_expect_tx(fb, a.tile_bytes);
+            if (inject_skip(a.inject, i)) continue;   // self test: this stage never fills
             const int32_t tr = int32_t(t / a.tiles_c), tc = int32_t(t % a.tiles_c);
             if (hint_load)
                 ptx::tma_load_2d_hint(ring_base + s * a.tile_bytes, &src_map, fb, tc * a.tile_cols,
