@@ -194,6 +194,28 @@ int gbr_copy_tuning(int store_lag, int ctas_per_sm, int l2_hint);
 int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage);
 
 /*
+ * Split tail of the tensor-core GEMMs (dense and grouped), for all later calls
+ * in the process.  A persistent launch runs T output tiles on U units (CTAs,
+ * or CTA pairs); the last T mod U tiles would make a final round that leaves
+ * the other units idle.  With the split on, the k-blocks of those tiles are
+ * dealt out in equal runs to all U units (at most 4 units share a tile).  Of
+ * the units sharing a tile, all but the last to arrive add their fp32 partial
+ * sums into a zeroed fp32 copy of the tile (reductions at L2) and count
+ * themselves done; the last to arrive waits, with the pipeline time limit,
+ * for those counts -- its partners have all started and finish without
+ * waiting on anything -- adds the copy to its own accumulator and runs the
+ * bias + ReLU epilogue.  Scratch (per call, stream-ordered, zeroed on the
+ * stream, from a memory pool the library keeps per device): (T mod U) x tile
+ * rows x 256 x 4 bytes plus counters.  Results differ from the unsplit kernel
+ * only by the order of fp32 additions.
+ *   mode -1: auto (split when the last round shrinks by >= 1/8 of a tile),
+ *         0: never, 1: whenever some tile can be split.
+ * GBR_ERR_INVALID for other values.  The failure-detection self tests and
+ * gemm_bias_relu_tf32_noalloc never split.
+ */
+int gbr_gemm_split_tail(int mode);
+
+/*
  * Failure-detection self test: launches one CTA that waits, with the given
  * limit, on an mbarrier phase nothing will complete.  The wait gives up, the
  * kernel records a timeout and returns; gbr_device_status() then reports

@@ -35,6 +35,7 @@ SIGNATURES = {
     "gbr_set_wait_timeout_ns": (_i32, [_u64]),
     "gbr_copy_tuning": (_i32, [_i32, _i32, _i32]),
     "gbr_gemm_tuning": (_i32, [_i32, _i32, _i32, _i32]),
+    "gbr_gemm_split_tail": (_i32, [_i32]),
     "gbr_selftest_wait_timeout": (_i32, [_u64, _vp]),
     "gbr_selftest_gemm_skip_load": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32,
                                            _i32, _u64, _vp]),
@@ -210,6 +211,12 @@ def gemm_tuning(cta_pair: int = -1, group_m: int = -1, l2_hint: int = -1,
     group_m raster band height in tiles; l2_hint operand-load L2 policy;
     k_per_stage 128-byte K slices per ring stage (see gbr.h)."""
     check(lib().gbr_gemm_tuning(int(cta_pair), int(group_m), int(l2_hint), int(k_per_stage)))
+
+
+def gemm_split_tail(mode: int = -1) -> None:
+    """Split the last round of tensor-core GEMM tiles along K: -1 auto, 0 never,
+    1 whenever possible (see gbr.h)."""
+    check(lib().gbr_gemm_split_tail(int(mode)))
 
 
 def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:

@@ -2,6 +2,7 @@
 // launch configuration and the device status block.
 #include "gbr.h"
 #include "gbr_internal.h"
+#include "split_plan.cuh"
 
 #include <cudaTypedefs.h>
 
@@ -34,6 +35,7 @@ int g_gemm_pair = -1;      // -1 auto, 1 one CTA per tile, 2 CTA pair per tile
 int g_gemm_group_m = -1;   // -1 auto: tile rows per raster band
 int g_gemm_l2_hint = -1;   // -1 auto (none): L2 policy of the operand loads
 int g_gemm_k_sub = -1;     // -1 auto (1): 128-byte K slices per ring stage
+int g_gemm_split = -1;     // -1 auto, 0 off, 1 on whenever some tile can be split
 
 constexpr int kMaxDevices = 64;
 
@@ -42,6 +44,7 @@ struct DevCtx {
     int sm_count = 0;
     int smem_optin = 0;
     uint32_t* status = nullptr;
+    cudaMemPool_t pool = nullptr;   // stream-ordered scratch; keeps what it maps
     bool ffma_regs_ok = false, ffma_regs_checked = false;
     bool umma_regs_ok[2][2][2] = {};        // [kind][grouped][pair - 1]
     bool umma_regs_checked[2][2][2] = {};
@@ -119,6 +122,21 @@ int get_ctx(DevCtx** out, int* dev_out = nullptr) {
             return cuda_fail(e, "cudaMalloc(status block)");
         if ((e = cudaMemset(c.status, 0, kStatusWords * sizeof(uint32_t))) != cudaSuccess)
             return cuda_fail(e, "cudaMemset(status block)");
+        // A pool of this library's own for per-call scratch (the TF32 B
+        // transpose, split-tile partial sums): allocation and release are
+        // stream-ordered, so calls on different streams never share scratch,
+        // and the pool keeps the memory it has mapped for the next call.
+        cudaMemPoolProps props;
+        memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if ((e = cudaMemPoolCreate(&c.pool, &props)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemPoolCreate");
+        uint64_t keep = ~0ull;
+        if ((e = cudaMemPoolSetAttribute(c.pool, cudaMemPoolAttrReleaseThreshold, &keep)) !=
+            cudaSuccess)
+            return cuda_fail(e, "cudaMemPoolSetAttribute");
         c.ready = true;
     }
     *out = &c;
@@ -269,6 +287,35 @@ int choose_pair(int64_t rows, int stages, int smem_optin, int* pair) {
     return GBR_OK;
 }
 
+// Fills the split fields of `s` (see split_plan.cuh); returns the scratch
+// bytes the launch needs (0: no split).
+size_t plan_split(GemmShape& s, int64_t units, int pair) {
+    int mode;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        mode = g_gemm_split;
+    }
+    return plan_split_fields(s, units, mode) ? split_scratch_bytes(s, pair) : 0;
+}
+
+// Scratch of one split launch from the device's pool, zeroed on the stream:
+// the counters, then the tiles' sums.
+int split_scratch(const DevCtx& c, GemmShape& s, int pair, size_t bytes, cudaStream_t st,
+                  void** ws) {
+    *ws = nullptr;
+    if (bytes == 0) return GBR_OK;
+    cudaError_t e = cudaMallocFromPoolAsync(ws, bytes, c.pool, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync(split-tile scratch)");
+    if ((e = cudaMemsetAsync(*ws, 0, bytes, st)) != cudaSuccess) {
+        cudaFreeAsync(*ws, st);
+        *ws = nullptr;
+        return cuda_fail(e, "cudaMemsetAsync(split-tile scratch)");
+    }
+    s.sk_count = static_cast<uint32_t*>(*ws);
+    s.sk_sum = reinterpret_cast<float*>(static_cast<uint8_t*>(*ws) + split_count_bytes(s, pair));
+    return GBR_OK;
+}
+
 int group_m_for(int pair) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_gemm_group_m > 0) return g_gemm_group_m;
@@ -354,6 +401,14 @@ int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage) {
     g_gemm_group_m = group_m;
     g_gemm_l2_hint = l2_hint;
     g_gemm_k_sub = k_per_stage;
+    return GBR_OK;
+}
+
+int gbr_gemm_split_tail(int mode) {
+    if (mode < -1 || mode > 1)
+        return fail(GBR_ERR_INVALID, "gbr_gemm_split_tail: mode must be -1, 0 or 1");
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_gemm_split = mode;
     return GBR_OK;
 }
 
@@ -641,7 +696,9 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
     const size_t smem = umma_smem_bytes(stages, pair, int(s.k_sub));
     if ((e = umma_prepare(kind, false, pair, smem)) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(tcgen05 GEMM)");
-    const int grid = pair * int(std::min<int64_t>(s.num_tiles, c->sm_count / pair));
+    const int64_t units = c->sm_count / pair;
+    const size_t split_bytes = plan_split(s, units, pair);
+    const int grid = pair * int(split_bytes ? units : std::min<int64_t>(s.num_tiles, units));
     float* bt = nullptr;  // TF32 only: K-major copy of B, stream-ordered scratch
     if (K > 0) {
         if ((r = encode_2d(&ma, dt, A, uint64_t(K), uint64_t(M), uint64_t(K) * es, bk, 128,
@@ -652,9 +709,9 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
                                bk, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != GBR_OK)
                 return r;
         } else {
-            if ((e = cudaMallocAsync(reinterpret_cast<void**>(&bt), size_t(K) * size_t(N) * 4, st)) !=
-                cudaSuccess)
-                return cuda_fail(e, "cudaMallocAsync(TF32 B transpose)");
+            if ((e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&bt),
+                                             size_t(K) * size_t(N) * 4, c->pool, st)) != cudaSuccess)
+                return cuda_fail(e, "cudaMallocFromPoolAsync(TF32 B transpose)");
             if ((r = encode_2d(&mb, dt, bt, uint64_t(K), uint64_t(N), uint64_t(K) * es, bk,
                                uint32_t(kUmmaBN / pair), CU_TENSOR_MAP_SWIZZLE_128B,
                                "Bt")) != GBR_OK) {
@@ -672,7 +729,13 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
         ma = mc;  // never read: no k-blocks are loaded when K == 0
         mb = mc;
     }
+    void* ws = nullptr;
+    if ((r = split_scratch(*c, s, pair, split_bytes, st, &ws)) != GBR_OK) {
+        if (bt) cudaFreeAsync(bt, st);
+        return r;
+    }
     e = launch_gemm_umma(kind, pair, ma, mb, mc, s, grid, smem, st);
+    if (ws) cudaFreeAsync(ws, st);
     if (bt) cudaFreeAsync(bt, st);
     if (e != cudaSuccess) return cuda_fail(e, "launching tcgen05 GEMM");
     ++g_launches;
@@ -805,10 +868,15 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
     const size_t smem = umma_smem_bytes(stages, pair, int(s.k_sub));
     cudaError_t e = umma_prepare(kUmmaBf16, true, pair, smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(grouped GEMM)");
-    const int grid = pair * int(std::min<int64_t>(s.num_tiles, c->sm_count / pair));
-    if ((e = launch_gemm_umma_grouped(pair, mx, mw, mc, g, s, int64_t(N), grid, smem,
-                                      reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
-        return cuda_fail(e, "launching grouped GEMM");
+    const int64_t units = c->sm_count / pair;
+    const size_t split_bytes = plan_split(s, units, pair);
+    const int grid = pair * int(split_bytes ? units : std::min<int64_t>(s.num_tiles, units));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    void* ws = nullptr;
+    if ((r = split_scratch(*c, s, pair, split_bytes, st, &ws)) != GBR_OK) return r;
+    e = launch_gemm_umma_grouped(pair, mx, mw, mc, g, s, int64_t(N), grid, smem, st);
+    if (ws) cudaFreeAsync(ws, st);
+    if (e != cudaSuccess) return cuda_fail(e, "launching grouped GEMM");
     ++g_launches;
     return GBR_OK;
 }

@@ -21,6 +21,7 @@ enum WaitSite : uint32_t {
     kSiteMmaAccEmpty = 0x32,
     kSiteMmaDrain = 0x33,
     kSiteEpiAccFull = 0x41,
+    kSiteEpiSplitSum = 0x42,
     kSiteStorerFull = 0x51,
     kSiteSelfTest = 0x71,
 };
@@ -99,6 +100,24 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if (ptx::globaltimer() - t0 > limit_ns) return false;
     }
+    return false;
+}
+
+// Bounded wait (one thread) until the global counter reaches `target`; the
+// writers are CTAs of the same launch that have already started, and they
+// increment the counter without waiting on anything.
+__device__ __forceinline__ bool counter_wait(const uint32_t* counter, uint32_t target,
+                                             const KernelCtl& ctl, volatile int* abort_flag,
+                                             uint32_t site, uint32_t item) {
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t iter = 0; iter < kMaxPollIters; ++iter) {
+        if (ptx::ld_acquire_gpu_u32(counter) >= target) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > ctl.timeout_ns) break;
+        __nanosleep(100);
+    }
+    *abort_flag = 1;
+    record_timeout(ctl, site, item);
     return false;
 }
 

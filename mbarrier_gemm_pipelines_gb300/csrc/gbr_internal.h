@@ -74,6 +74,18 @@ struct GemmShape {
                                    // evict_last, 2 A evict_first / B evict_last,
                                    // 3 A evict_last / B evict_first, 4 both evict_normal
     FaultInjection inject;         // failure-detection self test only (zeroed: none)
+    // Split tail (tensor-core GEMM; all zero: off, every tile runs whole).
+    // The first dp_tiles tiles (a multiple of the unit count) run whole, one
+    // per unit per round; the k-blocks of the last sk_tiles tiles, taken in
+    // (tile, k-block) order, are dealt out in runs of sk_iters to the units.
+    // Of the units sharing a tile, all but the last to arrive add their fp32
+    // part into the tile's sum in sk_sum; the last waits for them on
+    // sk_count, adds the sum to its own part and runs the epilogue.
+    int32_t dp_tiles;
+    int32_t sk_tiles;
+    int32_t sk_iters;
+    float* sk_sum;                 // [sk_tiles][tile rows][256] fp32, zeroed
+    uint32_t* sk_count;            // [sk_tiles][CTAs per tile][4 epilogue warps][2], zeroed
 };
 
 // FFMA path (strict fp32, CUDA cores): 128x128x32 tiles.

@@ -418,6 +418,21 @@ __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar, uint16_t
 }
 
 // ---------------------------------------------------------------- smem vectors
+// Load with acquire semantics at GPU scope (pairs with a release or with a
+// fence before the writer's atomic).
+__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t* addr) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
+// Four fp32 additions to global memory, performed at L2, no value returned.
+__device__ __forceinline__ void red_add_v4_f32(float4* addr, float a, float b, float c, float d) {
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a),
+                 "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),

@@ -51,6 +51,7 @@
 // bf16     64   16
 // tf32     32    8
 #include "gbr_internal.h"
+#include "split_plan.cuh"
 
 #include <cuda_bf16.h>
 
@@ -184,6 +185,52 @@ __device__ __forceinline__ TileInfo decode_tile(const UmmaParams<GROUPED>& P, ui
     return ti;
 }
 
+// Sum of split tile sk, the block of epilogue warp q of CTA `rank`: its 32
+// rows x 256 columns as [column / 4][lane] float4s, so that one warp
+// instruction touches 512 contiguous bytes.
+template <int PAIR>
+__device__ __forceinline__ float4* sum_block(const GemmShape& s, int32_t sk, uint32_t rank,
+                                             uint32_t q) {
+    const size_t blk = (size_t(sk) * PAIR + rank) * 4u + q;
+    return reinterpret_cast<float4*>(s.sk_sum) + blk * (kUmmaBN / 4u) * 32u;
+}
+
+// Adds columns [c, c + 32) of this lane's row to the tile's sum (at L2).
+__device__ __forceinline__ void sum_add32(float4* blk, uint32_t c, uint32_t lane,
+                                          const uint32_t (&r)[32]) {
+#pragma unroll
+    for (uint32_t i = 0; i < 8; ++i)
+        ptx::red_add_v4_f32(blk + (c / 4u + i) * 32u + lane, __uint_as_float(r[4 * i]),
+                            __uint_as_float(r[4 * i + 1]), __uint_as_float(r[4 * i + 2]),
+                            __uint_as_float(r[4 * i + 3]));
+}
+
+// Adds columns [c, c + 32) of this lane's row of the tile's sum, read at L2.
+__device__ __forceinline__ void sum_accum32(const float4* blk, uint32_t c, uint32_t lane,
+                                            uint32_t (&r)[32]) {
+#pragma unroll
+    for (uint32_t i = 0; i < 8; ++i) {
+        const float4 v = __ldcg(blk + (c / 4u + i) * 32u + lane);
+        r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) + v.x);
+        r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) + v.y);
+        r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) + v.z);
+        r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) + v.w);
+    }
+}
+
+// The epilogue warp is done reading accumulator buffer `ae` belongs to.
+template <int PAIR>
+__device__ __forceinline__ void acc_release(uint32_t ae, uint32_t lane) {
+    ptx::tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) {
+        if (PAIR == 2)
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(ae, 0));
+        else
+            ptx::mbar_arrive(ae);
+    }
+}
+
 template <int KIND, bool GROUPED, int PAIR, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_umma_kernel(const __grid_constant__ UmmaParams<GROUPED> P) {
@@ -260,10 +307,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_b = s.l2_hint == 3 ? pol_first : s.l2_hint == 4 ? pol_normal : pol_last;
             uint32_t it = 0;
             bool ok = true;
-            for (uint32_t t = unit; ok && t < uint32_t(s.num_tiles); t += units) {
-                const TileInfo ti = decode_tile<GROUPED, PAIR>(P, t, rank);
+            WorkItem w;
+            for (uint32_t j = 0; ok && work_item(s, unit, units, j, w); ++j) {
+                const TileInfo ti = decode_tile<GROUPED, PAIR>(P, w.tile, rank);
                 const int32_t bcol0 = ti.n0 + int32_t(rank * PR::b_cols);
-                for (int kb = 0; kb < s.num_kb; ++kb, ++it) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const uint32_t slot = it % S, ph = (it / S) & 1u;
                     if (!mbar_wait<kCl>(ptx::smem_addr(empty + slot), ph ^ 1u, s.ctl, abort_flag,
                                         kSiteProducerEmpty, it)) {
@@ -309,14 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ring_base = ptx::smem_addr(ring);
             uint32_t it = 0, tl = 0;
             bool ok = true;
-            for (uint32_t t = unit; ok && t < uint32_t(s.num_tiles); t += units, ++tl) {
+            WorkItem w;
+            for (; ok && work_item(s, unit, units, tl, w); ++tl) {
                 const uint32_t a = tl & 1u, aph = (tl >> 1) & 1u;
                 if (!mbar_wait<kCl>(ptx::smem_addr(acc_empty + a), aph ^ 1u, s.ctl, abort_flag,
                                     kSiteMmaAccEmpty, tl))
                     break;
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + a * kAccCols;
-                for (int kb = 0; kb < s.num_kb; ++kb, ++it) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const uint32_t slot = it % S, ph = (it / S) & 1u;
                     if (!mbar_wait<kCl>(ptx::smem_addr(full + slot), ph, s.ctl, abort_flag,
                                         kSiteMmaFull, it)) {
@@ -336,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             K_::b_kmajor
                                 ? sw128_desc(b_base + k * K_::mma_k * K_::esize, 16, 1024)
                                 : sw128_desc(b_base + k * K_::mma_k * 128, kPanelBytes, 1024);
-                        const uint32_t acc = (uint32_t(kb) | h | k) != 0;
+                        const uint32_t acc = (uint32_t(kb - w.kb0) | h | k) != 0;
                         if (PAIR == 2) {
                             if (KIND == kUmmaBf16)
                                 ptx::mma_f16_pair(d_tmem, ad, bd, kIdesc, acc);
@@ -356,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::mma_commit(ptx::smem_addr(empty + slot));
                 }
                 if (!ok) break;
-                if (s.num_kb > 0) {
+                if (w.kb1 > w.kb0) {
                     if (PAIR == 2)
                         ptx::mma_commit_pair_multicast(ptx::smem_addr(acc_full + a), 0x3);
                     else
@@ -386,15 +435,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage0 = ptx::smem_addr(epi) + q * 2u * kEpiBufBytes;
         const uint32_t row_off = lane * 128u;
         const uint32_t swz = lane & 7u;
-        const bool zero_acc = s.num_kb == 0;
-        uint32_t tl = 0, chunk_ctr = 0;
-        for (uint32_t t = unit; t < uint32_t(s.num_tiles); t += units, ++tl) {
-            const TileInfo ti = decode_tile<GROUPED, PAIR>(P, t, rank);
+        uint32_t chunk_ctr = 0;
+        WorkItem w;
+        for (uint32_t tl = 0; work_item(s, unit, units, tl, w); ++tl) {
+            const TileInfo ti = decode_tile<GROUPED, PAIR>(P, w.tile, rank);
             const uint32_t a = tl & 1u, aph = (tl >> 1) & 1u;
+            const uint32_t ae = ptx::smem_addr(acc_empty + a);
             if (!mbar_wait_warp<kCl>(ptx::smem_addr(acc_full + a), aph, s.ctl, abort_flag,
                                      kSiteEpiAccFull, tl))
                 break;
             ptx::tc_fence_after_sync();
+            const bool zero_acc = w.kb1 == w.kb0;
+            // Split tile: each unit sharing it checks in on arrival.  All but
+            // the last to arrive add their fp32 part of these 32 rows into the
+            // tile's zeroed sum (reductions at L2), free the accumulator and
+            // count themselves done.  The last to arrive waits until the
+            // others are done -- they have all started, and they finish
+            // without waiting on anything -- then adds the sum to its own
+            // accumulator in the epilogue below.
+            const float4* sum = nullptr;
+            if (w.parts > 1) {
+                float4* blk = sum_block<PAIR>(s, w.sk, rank, q);
+                uint32_t* arrived = s.sk_count + ((uint32_t(w.sk) * PAIR + rank) * 4u + q) * 2u;
+                uint32_t before = 0;
+                if (lane == 0) before = atomicAdd(arrived, 1u);
+                before = __shfl_sync(0xffffffffu, before, 0);
+                if (before + 1u != uint32_t(w.parts)) {
+                    const uint32_t acc0 = tmem_base + lane_base + a * kAccCols;
+#pragma unroll 1
+                    for (uint32_t c2 = 0; c2 < kAccCols; c2 += 64) {
+                        uint32_t r0[32], r1[32];
+                        ptx::tmem_ld_32x32b_x32(acc0 + c2, r0);
+                        ptx::tmem_ld_32x32b_x32(acc0 + c2 + 32, r1);
+                        ptx::tmem_ld_wait();
+                        sum_add32(blk, c2, lane, r0);
+                        sum_add32(blk, c2 + 32, lane, r1);
+                    }
+                    acc_release<PAIR>(ae, lane);
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) atomicAdd(arrived + 1, 1u);
+                    continue;
+                }
+                bool ok = true;
+                if (lane == 0)
+                    ok = counter_wait(arrived + 1, uint32_t(w.parts - 1), s.ctl, abort_flag,
+                                      kSiteEpiSplitSum, tl);
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+                __threadfence();
+                sum = blk;
+            }
             const float* bias = s.bias + (GROUPED ? P.bias_group_stride * ti.group : 0);
             const CUtensorMap* mapC = &P.mapC[GROUPED ? ti.group : 0];
             for (uint32_t c = 0; c < kChunks; ++c, ++chunk_ctr) {
@@ -406,16 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_32x32b_x32(taddr, r0);
                     ptx::tmem_ld_32x32b_x32(taddr + 32, r1);
                     ptx::tmem_ld_wait();
-                    if (c + 1 == kChunks) {
-                        ptx::tc_fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) {
-                            const uint32_t ae = ptx::smem_addr(acc_empty + a);
-                            if (PAIR == 2)
-                                ptx::mbar_arrive_cluster(ptx::mapa_shared(ae, 0));
-                            else
-                                ptx::mbar_arrive(ae);
-                        }
+                    if (c + 1 == kChunks) acc_release<PAIR>(ae, lane);
+                    if (sum != nullptr) {
+                        sum_accum32(sum, col0, lane, r0);
+                        sum_accum32(sum, col0 + 32, lane, r1);
                     }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -441,17 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t r0[32];
                     ptx::tmem_ld_32x32b_x32(taddr, r0);
                     ptx::tmem_ld_wait();
-                    if (c + 1 == kChunks) {
-                        ptx::tc_fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) {
-                            const uint32_t ae = ptx::smem_addr(acc_empty + a);
-                            if (PAIR == 2)
-                                ptx::mbar_arrive_cluster(ptx::mapa_shared(ae, 0));
-                            else
-                                ptx::mbar_arrive(ae);
-                        }
-                    }
+                    if (c + 1 == kChunks) acc_release<PAIR>(ae, lane);
+                    if (sum != nullptr) sum_accum32(sum, col0, lane, r0);
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
                         const int n = ti.n0 + int(col0) + 4 * j4;

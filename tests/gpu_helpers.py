@@ -68,3 +68,19 @@ class tuned:
     def __exit__(self, *exc):
         self.gbr.gemm_tuning(-1, -1, -1, -1)
         return False
+
+
+class split_tail:
+    """Sets the tensor-core GEMMs' split-tail mode (-1 auto, 0 never, 1 whenever
+    possible) for the duration of a with-block, then restores auto."""
+
+    def __init__(self, gbr, mode):
+        self.gbr, self.mode = gbr, mode
+
+    def __enter__(self):
+        self.gbr.gemm_split_tail(self.mode)
+        return self
+
+    def __exit__(self, *exc):
+        self.gbr.gemm_split_tail(-1)
+        return False

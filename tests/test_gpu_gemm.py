@@ -11,7 +11,7 @@ import torch
 import oracle
 from mbarrier_gemm_pipelines_gb300 import inputs
 from gpu_helpers import (TOL, load_library, rel_frobenius, require_gpu, sample_points,
-                         to_host_f64, tuned)
+                         split_tail, to_host_f64, tuned)
 
 pytestmark = pytest.mark.gpu
 
@@ -100,6 +100,36 @@ def test_pair_and_single_agree(gbr, dtype):
             outs.append(_run(gbr, A, B, bias, dtype, 3))
     assert rel_frobenius(outs[1], outs[0]) <= TOL[dtype] / 10
     _check_full(outs[1], A.float(), B.float(), bias, dtype)
+
+
+# Tile counts that leave a partial last round of units, K long enough to split:
+# a few tiles only (every unit runs a split run), more tiles than units (whole
+# tiles first, then the split round), ragged edges in M and N.
+SPLIT_SHAPES = [(383, 776, 1352), (520, 264, 4096), (130, 2056, 3000), (2304, 2304, 1024),
+                (256, 256, 8192)]
+
+
+@pytest.mark.parametrize("dtype,pair", [("tf32", 1), ("tf32", 2), ("bf16", 1), ("bf16", 2)])
+@pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
+def test_split_tail(gbr, dtype, pair, M, N, K):
+    """Last round split along K (forced on): parity with the oracle element by
+    element, and the unsplit kernel's result up to the order of fp32 additions."""
+    A, B, bias = inputs.gemm_normal(M, N, K, seed=M + N + K)
+    if dtype == "bf16":
+        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    with tuned(gbr, pair):
+        with split_tail(gbr, 1):
+            got = _run(gbr, A, B, bias, dtype, 3)
+        with split_tail(gbr, 0):
+            whole = _run(gbr, A, B, bias, dtype, 3)
+    _check_full(got, A.float(), B.float(), bias, dtype)
+    assert rel_frobenius(got, whole) <= TOL[dtype] / 10
+
+
+def test_split_tail_mode_is_validated(gbr):
+    with pytest.raises(gbr.GbrError):
+        gbr.gemm_split_tail(2)
+    gbr.gemm_split_tail(-1)
 
 
 def test_forced_single_rejects_deep_ring(gbr):

@@ -6,7 +6,8 @@ import torch
 
 import oracle
 from mbarrier_gemm_pipelines_gb300 import inputs
-from gpu_helpers import TOL, load_library, rel_frobenius, require_gpu, to_host_f64, tuned
+from gpu_helpers import (TOL, load_library, rel_frobenius, require_gpu, split_tail, to_host_f64,
+                         tuned)
 
 pytestmark = pytest.mark.gpu
 
@@ -39,11 +40,12 @@ def test_grouped_small(gbr, counts, K, N, pair):
 
 @pytest.mark.parametrize("pair", [1, 2])
 def test_grouped_matches_dense_per_expert(gbr, pair):
-    """Each expert's rows equal the dense kernel run on that expert alone."""
+    """Each expert's rows equal the dense kernel run on that expert alone (with
+    the split tail off both add the same products in the same order)."""
     counts = [200, 77, 300]
     cnt, X, W, b = inputs.grouped(tokens=sum(counts), experts=3, K=256, N=512, seed=11)
     dX, dW, db = X.cuda(), W.cuda(), b.cuda()
-    with tuned(gbr, pair):
+    with tuned(gbr, pair), split_tail(gbr, 0):
         C = gbr.gemm_bias_relu_grouped(dX, dW, db, counts, stages=4)
         off = 0
         for e, n_e in enumerate(counts):
@@ -52,6 +54,27 @@ def test_grouped_matches_dense_per_expert(gbr, pair):
             assert torch.equal(C[off:off + n_e], Ce)
             off += n_e
     gbr.check_device()
+
+
+@pytest.mark.parametrize("pair", [1, 2])
+def test_grouped_split_tail(gbr, pair):
+    """The last round split along K (forced on), tiles of several experts among
+    the split ones: parity with the oracle, and the unsplit result up to the
+    order of fp32 additions."""
+    counts = [300, 0, 513, 77, 1]
+    cnt, X, W, b = inputs.grouped(tokens=sum(counts), experts=5, K=1024, N=1032, seed=21)
+    dX, dW, db = X.cuda(), W.cuda(), b.cuda()
+    with tuned(gbr, pair):
+        with split_tail(gbr, 1):
+            C = gbr.gemm_bias_relu_grouped(dX, dW, db, counts, stages=3)
+        with split_tail(gbr, 0):
+            C0 = gbr.gemm_bias_relu_grouped(dX, dW, db, counts, stages=3)
+    gbr.check_device()
+    ref = oracle.gemm_bias_relu_grouped(X.float(), W.float(), b, counts)
+    got = to_host_f64(C)
+    assert rel_frobenius(got, ref) <= TOL["bf16"]
+    assert np.abs(got - ref).max() <= 0.2 * np.abs(ref).max()
+    assert rel_frobenius(got, to_host_f64(C0)) <= TOL["bf16"] / 10
 
 
 def test_grouped_rejects(gbr):
