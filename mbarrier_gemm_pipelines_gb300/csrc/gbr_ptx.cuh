@@ -418,6 +418,18 @@ __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar, uint16_t
 }
 
 // ---------------------------------------------------------------- smem vectors
+// Packed fp32 pair {lo, hi} in one 64-bit register.
+__device__ __forceinline__ uint64_t f32x2_splat(float x) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(x));
+    return d;
+}
+
+// d = a * b + d on both fp32 halves (each an IEEE fp32 fma, round to nearest).
+__device__ __forceinline__ void fma_f32x2(uint64_t& d, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
 // Load with acquire semantics at GPU scope (pairs with a release or with a
 // fence before the writer's atomic).
 __device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t* addr) {

@@ -32,14 +32,21 @@ constexpr uint32_t kConsumerRegs = 232;
 
 // One 32-deep K stage of the 128 x 128 tile for thread (tx, ty): rows
 // ty + 16 r, columns 4 tx .. 4 tx + 3 and 64 + 4 tx .. 64 + 4 tx + 3.  All of
-// the thread's rows share one swizzle phase per k-group and all its columns
-// one phase per k, read from the tables a_sw / b_sw, so every shared-memory
-// load is base + immediate offset.
-__device__ __forceinline__ void ffma_stage(float (&acc)[8][8], const uint8_t* As, const uint8_t* Bs,
-                                           const uint32_t (&a_sw)[8], const uint32_t (&b_sw)[8]) {
-#pragma unroll
+// the thread's rows share one swizzle phase (a_ph = ty % 8) per k-group, and
+// all its columns one phase per k, read from the table b_sw, so every
+// shared-memory load of a k-group is base + immediate offset.
+//
+// The accumulators are packed column pairs: acc[r][j] holds columns
+// (2j, 2j + 1) of the thread's eight, and each step is one packed fp32x2 FMA
+// (two IEEE fp32 FMAs, the same results as two scalar ones) of A broadcast to
+// both halves and a B pair read straight from shared memory as 64 bits.  Half
+// as many FMA instructions leave issue slots for the loads.
+__device__ __forceinline__ void ffma_stage(uint64_t (&acc)[8][4], const uint8_t* As,
+                                           const uint8_t* Bs, uint32_t a_row, uint32_t a_ph,
+                                           const uint32_t (&b_sw)[8]) {
+#pragma unroll 2
     for (uint32_t k4 = 0; k4 < kFfmaBK / 4; ++k4) {
-        const uint8_t* ap = As + a_sw[k4];
+        const uint8_t* ap = As + a_row + ((k4 ^ a_ph) << 4);   // row ty, 16-byte chunk k4
         float4 a[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) a[r] = *reinterpret_cast<const float4*>(ap + r * 16 * 128);
@@ -47,30 +54,39 @@ __device__ __forceinline__ void ffma_stage(float (&acc)[8][8], const uint8_t* As
         for (int kk = 0; kk < 4; ++kk) {
             const uint32_t k = 4 * k4 + kk;
             const uint8_t* bp = Bs + b_sw[k & 7u] + k * 128u;
-            const float4 b0 = *reinterpret_cast<const float4*>(bp);
-            const float4 b1 = *reinterpret_cast<const float4*>(bp + 2 * kBPanelBytes);
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(bp);
+            const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(bp + 2 * kBPanelBytes);
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const float av = kk == 0 ? a[r].x : kk == 1 ? a[r].y : kk == 2 ? a[r].z : a[r].w;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av, bv[c], acc[r][c]);
+                const uint64_t a2 = ptx::f32x2_splat(av);
+                ptx::fma_f32x2(acc[r][0], a2, b0.x);
+                ptx::fma_f32x2(acc[r][1], a2, b0.y);
+                ptx::fma_f32x2(acc[r][2], a2, b1.x);
+                ptx::fma_f32x2(acc[r][3], a2, b1.y);
             }
         }
     }
 }
 
-__device__ __forceinline__ void ffma_tables(uint32_t tx, uint32_t ty, uint32_t (&a_sw)[8],
-                                            uint32_t (&b_sw)[8]) {
+__device__ __forceinline__ void ffma_zero(uint64_t (&acc)[8][4]) {
 #pragma unroll
-    for (uint32_t j = 0; j < 8; ++j) {
-        a_sw[j] = ty * 128u + ((j ^ (ty & 7u)) << 4);                 // row ty, chunk j
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[r][j] = 0ull;
+}
+
+__device__ __forceinline__ void ffma_tables(uint32_t tx, uint32_t ty, uint32_t& a_row,
+                                            uint32_t& a_ph, uint32_t (&b_sw)[8]) {
+    a_row = ty * 128u;
+    a_ph = ty & 7u;
+#pragma unroll
+    for (uint32_t j = 0; j < 8; ++j)
         b_sw[j] = (tx >> 3) * kBPanelBytes + (((tx & 7u) ^ j) << 4);  // column 4 tx, K row % 8 = j
-    }
 }
 
 // C = max(0, acc + bias) for the thread's 8 x 8 outputs of tile (mt, nt).
-__device__ __forceinline__ void ffma_epilogue(const float (&acc)[8][8], const GemmShape& p,
+__device__ __forceinline__ void ffma_epilogue(const uint64_t (&acc)[8][4], const GemmShape& p,
                                               uint32_t mt, uint32_t nt, uint32_t tx, uint32_t ty) {
     float* C = static_cast<float*>(p.C);
     const int n0 = int(nt) * kFfmaBN, m0 = int(mt) * kFfmaBM;
@@ -83,11 +99,12 @@ __device__ __forceinline__ void ffma_epilogue(const float (&acc)[8][8], const Ge
         for (int r = 0; r < 8; ++r) {
             const int m = m0 + int(ty) + 16 * r;
             if (m >= p.M) continue;
+            const uint64_t lo = acc[r][2 * h], hi = acc[r][2 * h + 1];
             float4 v;
-            v.x = fmaxf(acc[r][4 * h + 0] + bb.x, 0.f);
-            v.y = fmaxf(acc[r][4 * h + 1] + bb.y, 0.f);
-            v.z = fmaxf(acc[r][4 * h + 2] + bb.z, 0.f);
-            v.w = fmaxf(acc[r][4 * h + 3] + bb.w, 0.f);
+            v.x = fmaxf(__uint_as_float(uint32_t(lo)) + bb.x, 0.f);
+            v.y = fmaxf(__uint_as_float(uint32_t(lo >> 32)) + bb.y, 0.f);
+            v.z = fmaxf(__uint_as_float(uint32_t(hi)) + bb.z, 0.f);
+            v.w = fmaxf(__uint_as_float(uint32_t(hi >> 32)) + bb.w, 0.f);
             *reinterpret_cast<float4*>(C + size_t(m) * p.N + n) = v;
         }
     }
@@ -164,19 +181,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // shared-memory load is base + immediate offset.
         const uint32_t ct = threadIdx.x - 128;        // 0..255
         const uint32_t tx = ct & 15u, ty = ct >> 4;
-        uint32_t a_sw[8], b_sw[8];
-        ffma_tables(tx, ty, a_sw, b_sw);
+        uint32_t a_row, a_ph, b_sw[8];
+        ffma_tables(tx, ty, a_row, a_ph, b_sw);
 
         uint32_t i = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
             uint32_t mt, nt;
             raster_tile(t, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
-            float acc[8][8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+            uint64_t acc[8][4];
+            ffma_zero(acc);
 
             for (int kb = 0; kb < p.num_kb; ++kb, ++i) {
                 const uint32_t s = i % S, ph = (i / S) & 1u;
@@ -186,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint8_t* As = ring + size_t(s) * kFfmaStageBytes;
-                ffma_stage(acc, As, As + kABytes, a_sw, b_sw);
+                ffma_stage(acc, As, As + kABytes, a_row, a_ph, b_sw);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(empty + s));
             }
@@ -218,13 +232,10 @@ __global__ void __launch_bounds__(kSyncThreads, 2) gemm_ffma_sync_kernel(const f
     uint32_t mt, nt;
     raster_tile(blockIdx.x, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
     const int m0 = int(mt) * kFfmaBM, n0 = int(nt) * kFfmaBN;
-    uint32_t a_sw[8], b_sw[8];
-    ffma_tables(tx, ty, a_sw, b_sw);
-    float acc[8][8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+    uint32_t a_row, a_ph, b_sw[8];
+    ffma_tables(tx, ty, a_row, a_ph, b_sw);
+    uint64_t acc[8][4];
+    ffma_zero(acc);
 
     for (int kb = 0; kb < p.num_kb; ++kb) {
         const int k0 = kb * kFfmaBK;
@@ -251,7 +262,7 @@ __global__ void __launch_bounds__(kSyncThreads, 2) gemm_ffma_sync_kernel(const f
                                        (((n4 & 7u) ^ (kr & 7u)) << 4)) = v;
         }
         __syncthreads();   // the whole tile has arrived
-        ffma_stage(acc, As, Bs, a_sw, b_sw);
+        ffma_stage(acc, As, Bs, a_row, a_ph, b_sw);
         __syncthreads();   // every thread is done with it
     }
     ffma_epilogue(acc, p, mt, nt, tx, ty);
