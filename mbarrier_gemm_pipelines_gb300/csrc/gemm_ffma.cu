@@ -44,7 +44,7 @@ constexpr uint32_t kConsumerRegs = 232;
 __device__ __forceinline__ void ffma_stage(uint64_t (&acc)[8][4], const uint8_t* As,
                                            const uint8_t* Bs, uint32_t a_row, uint32_t a_ph,
                                            const uint32_t (&b_sw)[8]) {
-#pragma unroll 2
+#pragma unroll
     for (uint32_t k4 = 0; k4 < kFfmaBK / 4; ++k4) {
         const uint8_t* ap = As + a_row + ((k4 ^ a_ph) << 4);   // row ty, 16-byte chunk k4
         float4 a[8];
