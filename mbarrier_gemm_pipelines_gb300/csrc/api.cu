@@ -289,18 +289,18 @@ int choose_pair(int64_t rows, int stages, int smem_optin, int* pair) {
 
 // Fills the split fields of `s` (see split_plan.cuh); returns the scratch
 // bytes the launch needs (0: no split).
-size_t plan_split(GemmShape& s, int64_t units, int pair) {
+size_t plan_split(GemmShape& s, int64_t units, SplitScratch kind) {
     int mode;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         mode = g_gemm_split;
     }
-    return plan_split_fields(s, units, mode) ? split_scratch_bytes(s, pair) : 0;
+    return plan_split_fields(s, units, mode) ? split_scratch_bytes(s, kind) : 0;
 }
 
 // Scratch of one split launch from the device's pool, zeroed on the stream:
 // the counters, then the tiles' sums.
-int split_scratch(const DevCtx& c, GemmShape& s, int pair, size_t bytes, cudaStream_t st,
+int split_scratch(const DevCtx& c, GemmShape& s, SplitScratch kind, size_t bytes, cudaStream_t st,
                   void** ws) {
     *ws = nullptr;
     if (bytes == 0) return GBR_OK;
@@ -312,7 +312,7 @@ int split_scratch(const DevCtx& c, GemmShape& s, int pair, size_t bytes, cudaStr
         return cuda_fail(e, "cudaMemsetAsync(split-tile scratch)");
     }
     s.sk_count = static_cast<uint32_t*>(*ws);
-    s.sk_sum = reinterpret_cast<float*>(static_cast<uint8_t*>(*ws) + split_count_bytes(s, pair));
+    s.sk_sum = reinterpret_cast<float*>(static_cast<uint8_t*>(*ws) + split_count_bytes(s, kind));
     return GBR_OK;
 }
 
@@ -697,7 +697,7 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
     if ((e = umma_prepare(kind, false, pair, smem)) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(tcgen05 GEMM)");
     const int64_t units = c->sm_count / pair;
-    const size_t split_bytes = plan_split(s, units, pair);
+    const size_t split_bytes = plan_split(s, units, umma_split_scratch(pair));
     const int grid = pair * int(split_bytes ? units : std::min<int64_t>(s.num_tiles, units));
     float* bt = nullptr;  // TF32 only: K-major copy of B, stream-ordered scratch
     if (K > 0) {
@@ -730,7 +730,7 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
         mb = mc;
     }
     void* ws = nullptr;
-    if ((r = split_scratch(*c, s, pair, split_bytes, st, &ws)) != GBR_OK) {
+    if ((r = split_scratch(*c, s, umma_split_scratch(pair), split_bytes, st, &ws)) != GBR_OK) {
         if (bt) cudaFreeAsync(bt, st);
         return r;
     }
@@ -869,11 +869,11 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
     cudaError_t e = umma_prepare(kUmmaBf16, true, pair, smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(grouped GEMM)");
     const int64_t units = c->sm_count / pair;
-    const size_t split_bytes = plan_split(s, units, pair);
+    const size_t split_bytes = plan_split(s, units, umma_split_scratch(pair));
     const int grid = pair * int(split_bytes ? units : std::min<int64_t>(s.num_tiles, units));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void* ws = nullptr;
-    if ((r = split_scratch(*c, s, pair, split_bytes, st, &ws)) != GBR_OK) return r;
+    if ((r = split_scratch(*c, s, umma_split_scratch(pair), split_bytes, st, &ws)) != GBR_OK) return r;
     e = launch_gemm_umma_grouped(pair, mx, mw, mc, g, s, int64_t(N), grid, smem, st);
     if (ws) cudaFreeAsync(ws, st);
     if (e != cudaSuccess) return cuda_fail(e, "launching grouped GEMM");

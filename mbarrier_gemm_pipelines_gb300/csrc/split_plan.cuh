@@ -18,6 +18,7 @@ namespace gbr {
 // kSplitMinRun k-blocks.
 constexpr int64_t kSplitMaxParts = 4;
 constexpr int64_t kSplitMinRun = 4;
+constexpr int64_t kSplitMinSaving = 8;   // auto: k-blocks the last round must shrink by
 
 // One unit of work of a persistent CTA (or CTA pair): k-blocks [kb0, kb1) of
 // output tile `tile`.  parts > 1: the tile is split along K among `parts`
@@ -77,8 +78,9 @@ __host__ __device__ __forceinline__ bool work_item(const GemmShape& s, uint32_t 
 inline int64_t split_cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Fills the split fields of `s` for `units` units (mode -1 auto: only when the
-// last round shrinks by at least an eighth of a tile; 1: whenever a tile can
-// be split; 0: never).  Returns true when the launch splits.
+// last round shrinks by at least an eighth of a tile and by kSplitMinSaving
+// k-blocks, so that small problems keep their single launch; 1: whenever a
+// tile can be split; 0: never).  Returns true when the launch splits.
 inline bool plan_split_fields(GemmShape& s, int64_t units, int mode) {
     s.dp_tiles = s.sk_tiles = s.sk_iters = 0;
     s.sk_sum = nullptr;
@@ -93,23 +95,30 @@ inline bool plan_split_fields(GemmShape& s, int64_t units, int mode) {
     if (run < run_parts) run = run_parts;
     if (run < run_min) run = run_min;
     if (run >= nkb) return false;
-    if (mode < 0 && run * 8 > nkb * 7) return false;
+    if (mode < 0 && (run * 8 > nkb * 7 || nkb - run < kSplitMinSaving)) return false;
     s.dp_tiles = int32_t(T - R);
     s.sk_tiles = int32_t(R);
     s.sk_iters = int32_t(run);
     return true;
 }
 
-// Scratch of a split launch, all zeroed before it: counters ([sk_tiles][pair]
-// [4 epilogue warps][arrived, done] words, padded to 256 bytes), then the
-// tiles' fp32 sums.
-inline size_t split_count_bytes(const GemmShape& s, int pair) {
-    return (size_t(s.sk_tiles) * size_t(pair) * 8u * sizeof(uint32_t) + 255u) & ~size_t(255);
+// Scratch of a split launch, all zeroed before it: `counters` words per split
+// tile (an arrived and a done count per epilogue warp), padded to 256 bytes,
+// then `sum_floats` fp32 per split tile (the tile's running sum).
+struct SplitScratch {
+    size_t counters;     // words per split tile
+    size_t sum_floats;   // floats per split tile
+};
+inline size_t split_count_bytes(const GemmShape& s, SplitScratch k) {
+    return (size_t(s.sk_tiles) * k.counters * sizeof(uint32_t) + 255u) & ~size_t(255);
 }
-inline size_t split_scratch_bytes(const GemmShape& s, int pair) {
+inline size_t split_scratch_bytes(const GemmShape& s, SplitScratch k) {
     if (s.sk_tiles == 0) return 0;
-    return split_count_bytes(s, pair) +
-           size_t(s.sk_tiles) * size_t(kUmmaBM * pair) * size_t(kUmmaBN) * 4u;
+    return split_count_bytes(s, k) + size_t(s.sk_tiles) * k.sum_floats * 4u;
+}
+// tcgen05 kernel: per CTA of the tile, 4 epilogue warps; 128 rows per CTA x 256.
+inline SplitScratch umma_split_scratch(int pair) {
+    return SplitScratch{size_t(pair) * 4u * 2u, size_t(kUmmaBM * pair) * size_t(kUmmaBN)};
 }
 
 }  // namespace gbr
