@@ -216,6 +216,25 @@ int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage);
 int gbr_gemm_split_tail(int mode);
 
 /*
+ * gemm_bias_relu_host -- gemm_bias_relu on HOST buffers: copies A, B and bias
+ * to the device, computes, and copies C back, overlapping the three.  The
+ * device buffers come from the library's stream-ordered pool.  M is cut into
+ * up to 8 chunks of whole 256-row tiles: B and bias are copied first, then
+ * chunk i of A is copied in while chunk i - 1 is computed and chunk i - 2 is
+ * copied out, on three streams of the library joined back into `stream`.
+ *   hA [M, K], hB [K, N], hC [M, N] (dtype as for gemm_bias_relu), hbias [N]
+ *   fp32: host memory owned by the caller; page-locked memory lets the copies
+ *   run asynchronously at full speed.  Stream-ordered: the call returns once
+ *   the work is enqueued; hC holds the result, and the inputs may be changed,
+ *   only after `stream` has reached that point (e.g. cudaStreamSynchronize).
+ *   Row pitches (K and N times the element size) must be multiples of 16
+ *   bytes.  Errors as for gemm_bias_relu; after a failed chunk the call still
+ *   joins its streams and frees its buffers before returning the error.
+ */
+int gemm_bias_relu_host(const void *hA, const void *hB, const float *hbias, void *hC, int64_t M,
+                        int64_t N, int64_t K, int dtype, int stages, gbr_stream_t stream);
+
+/*
  * Failure-detection self test: launches one CTA that waits, with the given
  * limit, on an mbarrier phase nothing will complete.  The wait gives up, the
  * kernel records a timeout and returns; gbr_device_status() then reports

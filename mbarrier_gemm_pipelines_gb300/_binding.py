@@ -26,6 +26,7 @@ _vp, _i64, _i32, _u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_
 SIGNATURES = {
     "gemm_bias_relu": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp]),
     "gemm_bias_relu_grouped": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _i32, _vp]),
+    "gemm_bias_relu_host": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp]),
     "staged_copy": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp]),
     "gbr_device_status": (_i32, [_vp]),
     "gbr_last_error": (ctypes.c_char_p, []),
@@ -125,6 +126,36 @@ def gemm_bias_relu(A, B, bias, C=None, dtype="bf16", stages=4, stream=None):
         raise ValueError("C must be [M, N]")
     check(lib().gemm_bias_relu(A.data_ptr(), B.data_ptr(), bias.data_ptr(), C.data_ptr(),
                                M, N, K, dt, int(stages), _stream_ptr(stream)))
+    return C
+
+
+def gemm_bias_relu_host(A, B, bias, C=None, dtype="bf16", stages=4, stream=None, sync=True):
+    """C = ReLU(A @ B + bias) for CPU tensors (page-locked for full copy speed):
+    the library copies in, computes and copies out, overlapped, on the current
+    CUDA device.  With sync=False the caller must synchronise `stream` before
+    reading C or changing the inputs."""
+    import torch
+    dt = DTYPE_NAMES[dtype] if isinstance(dtype, str) else int(dtype)
+    in_t = torch.bfloat16 if dt == BF16 else torch.float32
+    for t, n, want in ((A, "A", in_t), (B, "B", in_t), (bias, "bias", torch.float32)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda:
+            raise ValueError("%s must be a CPU tensor (host buffer)" % n)
+        if not t.is_contiguous() or t.dtype != want:
+            raise TypeError("%s must be contiguous %s" % (n, want))
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(bias.shape) != (N,):
+        raise ValueError("shape mismatch")
+    if C is None:
+        C = torch.empty((M, N), dtype=in_t).pin_memory()
+    if C.is_cuda or tuple(C.shape) != (M, N) or C.dtype != in_t or not C.is_contiguous():
+        raise ValueError("C must be a contiguous CPU [M, N] tensor of the input type")
+    s = _stream_ptr(stream)
+    check(lib().gemm_bias_relu_host(A.data_ptr(), B.data_ptr(), bias.data_ptr(), C.data_ptr(),
+                                    M, N, K, dt, int(stages), s))
+    if sync:
+        import torch as _t
+        (stream or _t.cuda.current_stream()).synchronize()
     return C
 
 

@@ -38,6 +38,8 @@ int g_gemm_k_sub = -1;     // -1 auto (1): 128-byte K slices per ring stage
 int g_gemm_split = -1;     // -1 auto, 0 off, 1 on whenever some tile can be split
 
 constexpr int kMaxDevices = 64;
+constexpr int kHostChunks = 8;                       // M chunks of a host-buffer GEMM
+constexpr int kHostEvents = 2 * kHostChunks + 2;     // fork, per chunk in/computed, join
 
 struct DevCtx {
     bool ready = false;
@@ -45,6 +47,12 @@ struct DevCtx {
     int smem_optin = 0;
     uint32_t* status = nullptr;
     cudaMemPool_t pool = nullptr;   // stream-ordered scratch; keeps what it maps
+    // Host-buffer GEMM: copy-in, compute and copy-out streams and their events,
+    // created on first use; one enqueue sequence at a time (host_mu).
+    bool host_ready = false;
+    cudaStream_t host_streams[3] = {};
+    cudaEvent_t host_events[kHostEvents] = {};
+    std::mutex host_mu;
     bool ffma_regs_ok = false, ffma_regs_checked = false;
     bool umma_regs_ok[2][2][2] = {};        // [kind][grouped][pair - 1]
     bool umma_regs_checked[2][2][2] = {};
@@ -878,6 +886,106 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
     if (ws) cudaFreeAsync(ws, st);
     if (e != cudaSuccess) return cuda_fail(e, "launching grouped GEMM");
     ++g_launches;
+    return GBR_OK;
+}
+
+// ------------------------------------------------------------ host buffers
+int gemm_bias_relu_host(const void* hA, const void* hB, const float* hbias, void* hC, int64_t M,
+                        int64_t N, int64_t K, int dtype, int stages, gbr_stream_t stream) {
+    if (dtype < GBR_F32_FFMA || dtype > GBR_F32_FFMA_SYNC)
+        return fail(GBR_ERR_INVALID, "gemm_bias_relu_host: unknown dtype %d", dtype);
+    const int64_t lim = int64_t(1) << 31;
+    if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim)
+        return fail(GBR_ERR_INVALID, "gemm_bias_relu_host: M, N, K must be in [0, 2^31)");
+    DevCtx* c;
+    int r = get_ctx(&c);
+    if (r != GBR_OK) return r;
+    const int smax = gemm_max_stages(dtype, c->smem_optin);
+    if (stages < 1 || stages > smax)
+        return fail(GBR_ERR_SMEM, "gemm_bias_relu_host: stages=%d outside [1, %d]", stages, smax);
+    if (M == 0 || N == 0) return GBR_OK;
+    if (!hC || !hbias || (K > 0 && (!hA || !hB)))
+        return fail(GBR_ERR_INVALID, "gemm_bias_relu_host: NULL buffer");
+    const size_t es = dtype == GBR_BF16 ? 2 : 4;
+    if ((size_t(N) * es) % 16 || (size_t(K) * es) % 16)
+        return fail(GBR_ERR_ALIGN, "gemm_bias_relu_host: row pitches must be multiples of 16 bytes");
+    auto up = [](size_t x) { return (x + 255u) & ~size_t(255); };
+    const size_t a_bytes = size_t(M) * size_t(K) * es, b_bytes = size_t(K) * size_t(N) * es;
+    const size_t bias_bytes = size_t(N) * 4, c_bytes = size_t(M) * size_t(N) * es;
+    const size_t off_b = up(a_bytes), off_bias = off_b + up(b_bytes), off_c = off_bias + up(bias_bytes);
+    const size_t total = off_c + up(c_bytes);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lk(c->host_mu);
+    cudaError_t e;
+    if (!c->host_ready) {
+        for (auto& hs : c->host_streams)
+            if ((e = cudaStreamCreateWithFlags(&hs, cudaStreamNonBlocking)) != cudaSuccess)
+                return cuda_fail(e, "cudaStreamCreateWithFlags");
+        for (auto& ev : c->host_events)
+            if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e, "cudaEventCreateWithFlags");
+        c->host_ready = true;
+    }
+    cudaStream_t s_in = c->host_streams[0], s_cmp = c->host_streams[1], s_out = c->host_streams[2];
+    cudaEvent_t* ev = c->host_events;
+    void* ws = nullptr;
+    if ((e = cudaMallocFromPoolAsync(&ws, total, c->pool, st)) != cudaSuccess)
+        return cuda_fail(e, "cudaMallocFromPoolAsync(host GEMM buffers)");
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    uint8_t *dA = base, *dB = base + off_b, *dC = base + off_c;
+    float* dbias = reinterpret_cast<float*>(base + off_bias);
+
+    // M in chunks (multiples of 256 rows): chunk i computes while chunk i + 1
+    // is copied in and chunk i - 1 is copied out.  B and bias go first.
+    const int64_t want = std::max<int64_t>(1, std::min<int64_t>(kHostChunks, M / 1024));
+    const int64_t rows = std::max<int64_t>(256, (cdiv(M, want) + 255) / 256 * 256);
+    const int chunks = int(cdiv(M, rows));
+    int first_err = GBR_OK;
+    std::string first_msg;
+    auto note = [&](int code) {
+        if (code != GBR_OK && first_err == GBR_OK) {
+            first_err = code;
+            first_msg = t_last_error;
+        }
+    };
+    auto cu = [&](cudaError_t err, const char* what) {
+        if (err != cudaSuccess) note(cuda_fail(err, what));
+    };
+    cu(cudaEventRecord(ev[0], st), "cudaEventRecord(fork)");
+    for (cudaStream_t hs : {s_in, s_cmp, s_out}) cu(cudaStreamWaitEvent(hs, ev[0], 0), "fork");
+    cu(cudaMemcpyAsync(dbias, hbias, bias_bytes, cudaMemcpyHostToDevice, s_in), "copy bias in");
+    if (K > 0) cu(cudaMemcpyAsync(dB, hB, b_bytes, cudaMemcpyHostToDevice, s_in), "copy B in");
+    for (int i = 0; i < chunks; ++i) {
+        const int64_t r0 = int64_t(i) * rows, n = std::min<int64_t>(rows, M - r0);
+        cudaEvent_t in = ev[1 + 2 * i], done = ev[2 + 2 * i];
+        if (K > 0)
+            cu(cudaMemcpyAsync(dA + size_t(r0) * size_t(K) * es,
+                               static_cast<const uint8_t*>(hA) + size_t(r0) * size_t(K) * es,
+                               size_t(n) * size_t(K) * es, cudaMemcpyHostToDevice, s_in),
+               "copy A chunk in");
+        cu(cudaEventRecord(in, s_in), "cudaEventRecord(in)");
+        cu(cudaStreamWaitEvent(s_cmp, in, 0), "wait in");
+        if (first_err == GBR_OK)
+            note(gemm_bias_relu(dA + size_t(r0) * size_t(K) * es, dB, dbias,
+                                dC + size_t(r0) * size_t(N) * es, n, N, K, dtype, stages,
+                                reinterpret_cast<gbr_stream_t>(s_cmp)));
+        cu(cudaEventRecord(done, s_cmp), "cudaEventRecord(computed)");
+        cu(cudaStreamWaitEvent(s_out, done, 0), "wait computed");
+        cu(cudaMemcpyAsync(static_cast<uint8_t*>(hC) + size_t(r0) * size_t(N) * es,
+                           dC + size_t(r0) * size_t(N) * es, size_t(n) * size_t(N) * es,
+                           cudaMemcpyDeviceToHost, s_out),
+           "copy C chunk out");
+    }
+    // Join: the caller's stream continues once the last chunk is back on the
+    // host (it waited for every computation, which waited for every copy in).
+    cu(cudaEventRecord(ev[kHostEvents - 1], s_out), "cudaEventRecord(join)");
+    cu(cudaStreamWaitEvent(st, ev[kHostEvents - 1], 0), "join");
+    cu(cudaFreeAsync(ws, st), "cudaFreeAsync(host GEMM buffers)");
+    if (first_err != GBR_OK) {
+        t_last_error = first_msg;
+        return first_err;
+    }
     return GBR_OK;
 }
 
