@@ -454,7 +454,9 @@ def run_ours(args):
                      "frac": round(achieved / peaks.get(peak_key, FALLBACK_PEAKS[peak_key]), 4),
                      "traffic": recorded_traffic("gemm_umma_bf16"),
                      "peak_source": "%s %s (burst cuBLAS bf16); sustained %s" % (
-                         peak_src, peak_key, peaks.get("bf16_tflops_sustained"))},
+                         peak_src, peak_key, peaks.get("bf16_tflops_sustained")),
+                     "frac_of_sustained": (round(achieved / peaks["bf16_tflops_sustained"], 4)
+                                           if peaks.get("bf16_tflops_sustained") else None)},
         "e2e": {"value": round(flops * e2e_steps / t_e2e / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "steps": e2e_steps, "api": "gemm_bias_relu_host (C ABI, pinned host buffers)",
