@@ -235,6 +235,26 @@ int gemm_bias_relu_host(const void *hA, const void *hB, const float *hbias, void
                         int64_t N, int64_t K, int dtype, int stages, gbr_stream_t stream);
 
 /*
+ * gbr_trace_buffer -- event trace of the ring protocol, for all later launches
+ * of the staged copy, the FFMA GEMM and the tensor-core GEMMs in the process
+ * (buffer NULL: off, the default).  `buffer` is caller-owned device memory,
+ * 16-byte aligned, of `bytes` >= 8192 + 32768 bytes.  Layout:
+ *   [512 CTAs][4 roles] uint32 event counts (8192 bytes), then per (CTA, role)
+ *   a region of cap = (bytes - 8192) / 32768 records of 16 bytes:
+ *   { uint64 %globaltimer ns, uint32 item, uint8 role, event, slot, parity }.
+ * Roles: 0 producer (empty waits, loads issued), 1 consumer (full waits and
+ * slot releases: copy storer, first FFMA consumer warp, MMA lane), 2 first
+ * epilogue warp (accumulator full waits, releases), 3 MMA lane on the
+ * accumulator ring (empty waits, tile commits).  Events: 0 wait returned
+ * (item, slot, parity waited on), 1 issued (recorded before the loads or the
+ * commit), 2 released (recorded before the arrive or commit).  A role counts
+ * every event and writes the first `cap`; CTAs from 512 on record nothing.
+ * Each launch overwrites the counts of the CTAs it runs.  GBR_ERR_INVALID for
+ * a misaligned or too small buffer.
+ */
+int gbr_trace_buffer(void *buffer, uint64_t bytes);
+
+/*
  * Failure-detection self test: launches one CTA that waits, with the given
  * limit, on an mbarrier phase nothing will complete.  The wait gives up, the
  * kernel records a timeout and returns; gbr_device_status() then reports

@@ -37,6 +37,7 @@ SIGNATURES = {
     "gbr_copy_tuning": (_i32, [_i32, _i32, _i32]),
     "gbr_gemm_tuning": (_i32, [_i32, _i32, _i32, _i32]),
     "gbr_gemm_split_tail": (_i32, [_i32]),
+    "gbr_trace_buffer": (_i32, [_vp, _u64]),
     "gbr_selftest_wait_timeout": (_i32, [_u64, _vp]),
     "gbr_selftest_gemm_skip_load": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32,
                                            _i32, _u64, _vp]),

@@ -36,6 +36,8 @@ int g_gemm_group_m = -1;   // -1 auto: tile rows per raster band
 int g_gemm_l2_hint = -1;   // -1 auto (none): L2 policy of the operand loads
 int g_gemm_k_sub = -1;     // -1 auto (1): 128-byte K slices per ring stage
 int g_gemm_split = -1;     // -1 auto, 0 off, 1 on whenever some tile can be split
+uint8_t* g_trace = nullptr;  // event trace buffer (device memory of the caller), or null
+uint32_t g_trace_cap = 0;    // records per (CTA, role)
 
 constexpr int kMaxDevices = 64;
 constexpr int kHostChunks = 8;                       // M chunks of a host-buffer GEMM
@@ -156,6 +158,9 @@ KernelCtl make_ctl(const DevCtx& c) {
     KernelCtl k;
     k.status = c.status;
     k.timeout_ns = t_timeout_override ? t_timeout_override : timeout_ns();
+    std::lock_guard<std::mutex> lk(g_mu);
+    k.trace = g_trace;
+    k.trace_cap = g_trace_cap;
     return k;
 }
 
@@ -409,6 +414,24 @@ int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage) {
     g_gemm_group_m = group_m;
     g_gemm_l2_hint = l2_hint;
     g_gemm_k_sub = k_per_stage;
+    return GBR_OK;
+}
+
+int gbr_trace_buffer(void* buffer, uint64_t bytes) {
+    if (buffer == nullptr) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_trace = nullptr;
+        g_trace_cap = 0;
+        return GBR_OK;
+    }
+    const uint64_t region = uint64_t(kTraceMaxCtas) * kTraceRoles * 16u;
+    if (bytes < kTraceHeaderBytes + region || (reinterpret_cast<uintptr_t>(buffer) & 15u))
+        return fail(GBR_ERR_INVALID,
+                    "gbr_trace_buffer: need a 16-byte aligned buffer of at least %llu bytes",
+                    (unsigned long long)(kTraceHeaderBytes + region));
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_trace = static_cast<uint8_t*>(buffer);
+    g_trace_cap = uint32_t(std::min<uint64_t>((bytes - kTraceHeaderBytes) / region, 1u << 24));
     return GBR_OK;
 }
 

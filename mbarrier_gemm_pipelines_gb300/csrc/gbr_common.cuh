@@ -26,10 +26,56 @@ enum WaitSite : uint32_t {
     kSiteSelfTest = 0x71,
 };
 
-struct KernelCtl {
-    uint32_t* status;          // device status block (kStatusWords words)
-    uint64_t timeout_ns;       // per-wait limit on %globaltimer
+// Optional event trace (null: off).  Layout of the trace buffer:
+//   [kTraceMaxCtas][kTraceRoles] uint32 event counts (kTraceHeaderBytes), then
+//   per (CTA, role) a region of trace_cap 16-byte records
+//   { uint64 %globaltimer, uint32 item, uint8 role, event, slot, parity }.
+// A role counts every event; it writes the first trace_cap of them.
+constexpr uint32_t kTraceMaxCtas = 512;
+constexpr uint32_t kTraceRoles = 4;
+constexpr size_t kTraceHeaderBytes = size_t(kTraceMaxCtas) * kTraceRoles * 4;
+enum TraceRole : uint32_t {
+    kRoleProducer = 0,   // ring producer: waits on empty, issues TMA
+    kRoleConsumer = 1,   // ring consumer: FFMA warp, MMA lane or copy storer
+    kRoleEpilogue = 2,   // tcgen05 epilogue warp: waits on acc_full, frees acc_empty
+    kRoleMmaAcc = 3,     // tcgen05 MMA lane on the accumulator ring
 };
+enum TraceEvent : uint32_t {
+    kEvWaitDone = 0,     // a wait returned: (item, slot, parity waited on)
+    kEvIssued = 1,       // producer issued the stage's loads / MMA lane committed a tile
+    kEvReleased = 2,     // the slot's release is issued (arrive or commit follows)
+};
+
+struct KernelCtl {
+    uint32_t* status = nullptr;      // device status block (kStatusWords words)
+    uint64_t timeout_ns = 0;         // per-wait limit on %globaltimer
+    uint8_t* trace = nullptr;        // event trace buffer, or null
+    uint32_t trace_cap = 0;          // records per (CTA, role)
+};
+
+// Records one event of `role` (n: that role's running count in this CTA).
+__device__ __forceinline__ void trace_event(const KernelCtl& c, uint32_t role, uint32_t& n,
+                                            uint32_t ev, uint32_t item, uint32_t slot,
+                                            uint32_t parity) {
+    if (c.trace == nullptr || blockIdx.x >= kTraceMaxCtas) return;
+    if (n < c.trace_cap) {
+        const uint64_t t = ptx::globaltimer();
+        uint4 v;
+        v.x = uint32_t(t);
+        v.y = uint32_t(t >> 32);
+        v.z = item;
+        v.w = role | (ev << 8) | ((slot & 0xFFu) << 16) | ((parity & 0xFFu) << 24);
+        reinterpret_cast<uint4*>(c.trace + kTraceHeaderBytes)
+            [(size_t(blockIdx.x) * kTraceRoles + role) * c.trace_cap + n] = v;
+    }
+    ++n;
+}
+
+// Publishes a role's event count for this CTA.
+__device__ __forceinline__ void trace_count(const KernelCtl& c, uint32_t role, uint32_t n) {
+    if (c.trace != nullptr && blockIdx.x < kTraceMaxCtas)
+        reinterpret_cast<uint32_t*>(c.trace)[blockIdx.x * kTraceRoles + role] = n;
+}
 
 // Iteration cap of one bounded wait; the time limit normally ends it first.
 constexpr uint32_t kMaxPollIters = 1u << 26;

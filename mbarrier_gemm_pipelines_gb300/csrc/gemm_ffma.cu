@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::setmaxnreg_dec<kProducerRegs>();
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------ producer
-            uint32_t i = 0;
+            uint32_t i = 0, ntr = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
                 uint32_t mt, nt;
@@ -154,9 +154,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    trace_event(p.ctl, kRoleProducer, ntr, kEvWaitDone, i, s, ph ^ 1u);
                     const uint32_t fb = ptx::smem_addr(full + s);
                     ptx::mbar_arrive_expect_tx(fb, kFfmaStageBytes);
                     if (inject_skip(p.inject, i)) continue;   // self test: stage never fills
+                    trace_event(p.ctl, kRoleProducer, ntr, kEvIssued, i, s, 0);
                     const uint32_t st = ring_base + s * kFfmaStageBytes;
                     ptx::tma_load_2d(st, &mapA, fb, kb * kFfmaBK, int(mt) * kFfmaBM);
 #pragma unroll
@@ -165,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          int(nt) * kFfmaBN + 32 * j, kb * kFfmaBK);
                 }
             }
+            trace_count(p.ctl, kRoleProducer, ntr);
             if (*abort_flag) {
                 const uint32_t n = i < uint32_t(S) ? i : uint32_t(S);
                 for (uint32_t j = i - n; j < i; ++j)
@@ -186,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t a_row, a_ph, b_sw[8];
         ffma_tables(tx, ty, a_row, a_ph, b_sw);
 
-        uint32_t i = 0;
+        uint32_t i = 0, ntr = 0;
+        const bool tracer = p.ctl.trace != nullptr && warp == 4 && lane == 0;   // one consumer lane
         bool ok = true;
         for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
             uint32_t mt, nt;
@@ -201,15 +205,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                if (tracer) trace_event(p.ctl, kRoleConsumer, ntr, kEvWaitDone, i, s, ph);
                 const uint8_t* As = ring + size_t(s) * kFfmaStageBytes;
                 ffma_stage(acc, As, As + kABytes, a_row, a_ph, b_sw);
                 __syncwarp();
+                if (tracer) trace_event(p.ctl, kRoleConsumer, ntr, kEvReleased, i, s, 0);
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(empty + s));
             }
             if (!ok) break;
 
             ffma_epilogue(acc, p, mt, nt, tx, ty);
         }
+        if (tracer) trace_count(p.ctl, kRoleConsumer, ntr);
     }
     __syncwarp();
     __syncthreads();

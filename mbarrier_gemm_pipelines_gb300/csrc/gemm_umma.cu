@@ -231,7 +231,7 @@ __device__ __forceinline__ void acc_release(uint32_t ae, uint32_t lane) {
     }
 }
 
-template <int KIND, bool GROUPED, int PAIR, int KSUB>
+template <int KIND, bool GROUPED, int PAIR, int KSUB, bool TRACE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_umma_kernel(const __grid_constant__ UmmaParams<GROUPED> P) {
     using K_ = Kind<KIND>;
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_normal = ptx::l2_policy_evict_normal();
             const uint64_t pol_a = s.l2_hint == 2 ? pol_first : s.l2_hint == 4 ? pol_normal : pol_last;
             const uint64_t pol_b = s.l2_hint == 3 ? pol_first : s.l2_hint == 4 ? pol_normal : pol_last;
-            uint32_t it = 0;
+            uint32_t it = 0, ntr = 0;
             bool ok = true;
             WorkItem w;
             for (uint32_t j = 0; ok && work_item(s, unit, units, j, w); ++j) {
@@ -318,10 +318,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    if (TRACE) trace_event(s.ctl, kRoleProducer, ntr, kEvWaitDone, it, slot, ph ^ 1u);
                     const uint32_t fb_local = ptx::smem_addr(full + slot);
                     const uint32_t fb = PAIR == 2 ? ptx::mapa_shared(fb_local, 0) : fb_local;
                     if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, PAIR * stage_bytes);
                     if (PAIR == 1 && inject_skip(s.inject, it)) continue;   // self test
+                    if (TRACE) trace_event(s.ctl, kRoleProducer, ntr, kEvIssued, it, slot, 0);
                     const uint32_t stage_base = ring_base + slot * stage_bytes;
 #pragma unroll
                     for (uint32_t h = 0; h < ksub; ++h) {
@@ -347,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (TRACE) trace_count(s.ctl, kRoleProducer, ntr);
             if (*abort_flag && rank == 0) {
                 const uint32_t n = it < uint32_t(S) ? it : uint32_t(S);
                 for (uint32_t j = it - n; j < it; ++j)
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == 1 && lane == 0 && rank == 0) {
             // ---------------------------------------------------- MMA issuer
             const uint32_t ring_base = ptx::smem_addr(ring);
-            uint32_t it = 0, tl = 0;
+            uint32_t it = 0, tl = 0, ntr = 0, nta = 0;
             bool ok = true;
             WorkItem w;
             for (; ok && work_item(s, unit, units, tl, w); ++tl) {
@@ -363,6 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait<kCl>(ptx::smem_addr(acc_empty + a), aph ^ 1u, s.ctl, abort_flag,
                                     kSiteMmaAccEmpty, tl))
                     break;
+                if (TRACE) trace_event(s.ctl, kRoleMmaAcc, nta, kEvWaitDone, tl, a, aph ^ 1u);
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + a * kAccCols;
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
@@ -372,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    if (TRACE) trace_event(s.ctl, kRoleConsumer, ntr, kEvWaitDone, it, slot, ph);
                     ptx::tc_fence_after_sync();
                     const uint32_t stage_base = ring_base + slot * stage_bytes;
 #pragma unroll
@@ -399,12 +404,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     }
+                    if (TRACE) trace_event(s.ctl, kRoleConsumer, ntr, kEvReleased, it, slot, 0);
                     if (PAIR == 2)
                         ptx::mma_commit_pair_multicast(ptx::smem_addr(empty + slot), 0x3);
                     else
                         ptx::mma_commit(ptx::smem_addr(empty + slot));
                 }
                 if (!ok) break;
+                if (TRACE) trace_event(s.ctl, kRoleMmaAcc, nta, kEvIssued, tl, a, 0);
                 if (w.kb1 > w.kb0) {
                     if (PAIR == 2)
                         ptx::mma_commit_pair_multicast(ptx::smem_addr(acc_full + a), 0x3);
@@ -420,6 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (TRACE) trace_count(s.ctl, kRoleConsumer, ntr);
+            if (TRACE) trace_count(s.ctl, kRoleMmaAcc, nta);
             // No MMA may still be running when TMEM (or the peer's smem) is released.
             if (PAIR == 2)
                 ptx::mma_commit_pair_multicast(ptx::smem_addr(drain), 0x1);
@@ -435,7 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage0 = ptx::smem_addr(epi) + q * 2u * kEpiBufBytes;
         const uint32_t row_off = lane * 128u;
         const uint32_t swz = lane & 7u;
-        uint32_t chunk_ctr = 0;
+        uint32_t chunk_ctr = 0, ntr = 0;
+        const bool tracer = TRACE && q == 0 && lane == 0;   // one epilogue lane
         WorkItem w;
         for (uint32_t tl = 0; work_item(s, unit, units, tl, w); ++tl) {
             const TileInfo ti = decode_tile<GROUPED, PAIR>(P, w.tile, rank);
@@ -444,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait_warp<kCl>(ptx::smem_addr(acc_full + a), aph, s.ctl, abort_flag,
                                      kSiteEpiAccFull, tl))
                 break;
+            if (tracer) trace_event(s.ctl, kRoleEpilogue, ntr, kEvWaitDone, tl, a, aph);
             ptx::tc_fence_after_sync();
             const bool zero_acc = w.kb1 == w.kb0;
             // Split tile: each unit sharing it checks in on arrival.  All but
@@ -471,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sum_add32(blk, c2, lane, r0);
                         sum_add32(blk, c2 + 32, lane, r1);
                     }
+                    if (tracer) trace_event(s.ctl, kRoleEpilogue, ntr, kEvReleased, tl, a, 0);
                     acc_release<PAIR>(ae, lane);
                     __threadfence();
                     __syncwarp();
@@ -496,7 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_32x32b_x32(taddr, r0);
                     ptx::tmem_ld_32x32b_x32(taddr + 32, r1);
                     ptx::tmem_ld_wait();
-                    if (c + 1 == kChunks) acc_release<PAIR>(ae, lane);
+                    if (c + 1 == kChunks) {
+                        if (tracer) trace_event(s.ctl, kRoleEpilogue, ntr, kEvReleased, tl, a, 0);
+                        acc_release<PAIR>(ae, lane);
+                    }
                     if (sum != nullptr) {
                         sum_accum32(sum, col0, lane, r0);
                         sum_accum32(sum, col0 + 32, lane, r1);
@@ -525,7 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t r0[32];
                     ptx::tmem_ld_32x32b_x32(taddr, r0);
                     ptx::tmem_ld_wait();
-                    if (c + 1 == kChunks) acc_release<PAIR>(ae, lane);
+                    if (c + 1 == kChunks) {
+                        if (tracer) trace_event(s.ctl, kRoleEpilogue, ntr, kEvReleased, tl, a, 0);
+                        acc_release<PAIR>(ae, lane);
+                    }
                     if (sum != nullptr) sum_accum32(sum, col0, lane, r0);
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
@@ -558,6 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if (tracer) trace_count(s.ctl, kRoleEpilogue, ntr);
         if (lane == 0) ptx::bulk_wait_group<0>();
     }
 
@@ -576,24 +595,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int KIND, bool GROUPED, int PAIR, int KSUB>
+template <int KIND, bool GROUPED, int PAIR, int KSUB, bool TRACE>
 void* kernel_ptr() {
-    return reinterpret_cast<void*>(&gemm_umma_kernel<KIND, GROUPED, PAIR, KSUB>);
+    return reinterpret_cast<void*>(&gemm_umma_kernel<KIND, GROUPED, PAIR, KSUB, TRACE>);
+}
+
+// Instances with the event trace compiled in run only while a trace buffer is
+// set: the trace points cost the untraced kernels ~2% on the MMA lane.
+template <int KIND, bool GROUPED, bool TRACE>
+void* select_kernel_kgt(int pair, int ksub) {
+    if (pair == 2)
+        return ksub == 2 ? kernel_ptr<KIND, GROUPED, 2, 2, TRACE>()
+                         : kernel_ptr<KIND, GROUPED, 2, 1, TRACE>();
+    return ksub == 2 ? kernel_ptr<KIND, GROUPED, 1, 2, TRACE>()
+                     : kernel_ptr<KIND, GROUPED, 1, 1, TRACE>();
 }
 
 template <int KIND, bool GROUPED>
-void* select_kernel_kg(int pair, int ksub) {
-    if (pair == 2)
-        return ksub == 2 ? kernel_ptr<KIND, GROUPED, 2, 2>() : kernel_ptr<KIND, GROUPED, 2, 1>();
-    return ksub == 2 ? kernel_ptr<KIND, GROUPED, 1, 2>() : kernel_ptr<KIND, GROUPED, 1, 1>();
+void* select_kernel_kg(int pair, int ksub, bool trace) {
+    return trace ? select_kernel_kgt<KIND, GROUPED, true>(pair, ksub)
+                 : select_kernel_kgt<KIND, GROUPED, false>(pair, ksub);
 }
 
-void* select_kernel(int kind, bool grouped, int pair, int ksub) {
+void* select_kernel(int kind, bool grouped, int pair, int ksub, bool trace) {
     if (kind == kUmmaBf16)
-        return grouped ? select_kernel_kg<kUmmaBf16, true>(pair, ksub)
-                       : select_kernel_kg<kUmmaBf16, false>(pair, ksub);
-    return grouped ? select_kernel_kg<kUmmaTf32, true>(pair, ksub)
-                   : select_kernel_kg<kUmmaTf32, false>(pair, ksub);
+        return grouped ? select_kernel_kg<kUmmaBf16, true>(pair, ksub, trace)
+                       : select_kernel_kg<kUmmaBf16, false>(pair, ksub, trace);
+    return grouped ? select_kernel_kg<kUmmaTf32, true>(pair, ksub, trace)
+                   : select_kernel_kg<kUmmaTf32, false>(pair, ksub, trace);
 }
 
 int ksub_of(const GemmShape& s) { return s.k_sub == 2 ? 2 : 1; }
@@ -616,7 +645,8 @@ cudaError_t launch_umma(int kind, int pair, const UmmaParams<GROUPED>& P, int gr
     cfg.attrs = attr;
     cfg.numAttrs = pair == 2 ? 1 : 0;
     void* args[] = {const_cast<UmmaParams<GROUPED>*>(&P)};
-    return cudaLaunchKernelExC(&cfg, select_kernel(kind, GROUPED, pair, ksub_of(P.s)), args);
+    return cudaLaunchKernelExC(
+        &cfg, select_kernel(kind, GROUPED, pair, ksub_of(P.s), P.s.ctl.trace != nullptr), args);
 }
 
 }  // namespace
@@ -637,17 +667,19 @@ size_t umma_smem_bytes(int stages) { return umma_smem_bytes(stages, 1); }
 
 cudaError_t umma_prepare(int kind, bool grouped, int pair, size_t smem) {
     static std::mutex mu;
-    static size_t set[kMaxDeviceSlots][2][2][2][2] = {};   // [dev][kind][grouped][pair-1][ksub-1]
+    // [dev][kind][grouped][pair-1][ksub-1][trace]
+    static size_t set[kMaxDeviceSlots][2][2][2][2][2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDeviceSlots) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(mu);
-    for (int ksub = 1; ksub <= 2; ++ksub) {
-        e = raise_smem_limit(select_kernel(kind, grouped, pair, ksub), smem,
-                             &set[dev][kind][grouped ? 1 : 0][pair - 1][ksub - 1]);
-        if (e != cudaSuccess) return e;
-    }
+    for (int ksub = 1; ksub <= 2; ++ksub)
+        for (int tr = 0; tr < 2; ++tr) {
+            e = raise_smem_limit(select_kernel(kind, grouped, pair, ksub, tr != 0), smem,
+                                 &set[dev][kind][grouped ? 1 : 0][pair - 1][ksub - 1][tr]);
+            if (e != cudaSuccess) return e;
+        }
     return cudaSuccess;
 }
 cudaError_t umma_prepare(int kind, bool grouped, size_t smem) {
@@ -657,12 +689,14 @@ cudaError_t umma_prepare(int kind, bool grouped, size_t smem) {
 cudaError_t umma_check_registers(int kind, bool grouped, int pair, int* regs) {
     cudaFuncAttributes fa;
     const long need = 128L * kRegsWG0 + 128L * kRegsWG1;
-    for (int ksub = 1; ksub <= 2; ++ksub) {
-        cudaError_t e = cudaFuncGetAttributes(&fa, select_kernel(kind, grouped, pair, ksub));
-        if (e != cudaSuccess) return e;
-        *regs = fa.numRegs;
-        if (long(fa.numRegs) * kThreads < need) return cudaErrorInvalidConfiguration;
-    }
+    for (int ksub = 1; ksub <= 2; ++ksub)
+        for (int tr = 0; tr < 2; ++tr) {
+            cudaError_t e =
+                cudaFuncGetAttributes(&fa, select_kernel(kind, grouped, pair, ksub, tr != 0));
+            if (e != cudaSuccess) return e;
+            *regs = fa.numRegs;
+            if (long(fa.numRegs) * kThreads < need) return cudaErrorInvalidConfiguration;
+        }
     return cudaSuccess;
 }
 cudaError_t umma_check_registers(int kind, bool grouped, int* regs) {

@@ -49,15 +49,17 @@ __global__ void __launch_bounds__(64, 1)
     const bool hint_load = (a.l2_hint & 1u) != 0, hint_store = (a.l2_hint & 2u) != 0;
     if (warp == 0 && lane == 0) {
         // ---------------- producer: wait empty -> expect_tx -> TMA load
-        uint32_t i = 0;
+        uint32_t i = 0, nt = 0;
         for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x, ++i) {
             const uint32_t s = i % S, ph = (i / S) & 1u;
             if (!mbar_wait(ptx::smem_addr(empty + s), ph ^ 1u, a.ctl, abort_flag,
                            kSiteProducerEmpty, i))
                 break;
+            trace_event(a.ctl, kRoleProducer, nt, kEvWaitDone, i, s, ph ^ 1u);
             const uint32_t fb = ptx::smem_addr(full + s);
             ptx::mbar_arrive_expect_tx(fb, a.tile_bytes);
             if (inject_skip(a.inject, i)) continue;   // self test: this stage never fills
+            trace_event(a.ctl, kRoleProducer, nt, kEvIssued, i, s, 0);   // before the load lands
             const int32_t tr = int32_t(t / a.tiles_c), tc = int32_t(t % a.tiles_c);
             if (hint_load)
                 ptx::tma_load_2d_hint(ring_base + s * a.tile_bytes, &src_map, fb, tc * a.tile_cols,
@@ -66,6 +68,7 @@ __global__ void __launch_bounds__(64, 1)
                 ptx::tma_load_2d(ring_base + s * a.tile_bytes, &src_map, fb, tc * a.tile_cols,
                                  tr * a.tile_rows);
         }
+        trace_count(a.ctl, kRoleProducer, nt);
         if (*abort_flag) {
             // Let this CTA's own loads in flight land before the CTA exits.
             const uint32_t n = i < uint32_t(S) ? i : uint32_t(S);
@@ -74,11 +77,12 @@ __global__ void __launch_bounds__(64, 1)
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- storer: wait full -> TMA store -> release when read
-        uint32_t i = 0;
+        uint32_t i = 0, nt = 0;
         for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x, ++i) {
             const uint32_t s = i % S, ph = (i / S) & 1u;
             if (!mbar_wait(ptx::smem_addr(full + s), ph, a.ctl, abort_flag, kSiteStorerFull, i))
                 break;
+            trace_event(a.ctl, kRoleConsumer, nt, kEvWaitDone, i, s, ph);
             const int32_t tr = int32_t(t / a.tiles_c), tc = int32_t(t % a.tiles_c);
             if (hint_store)
                 ptx::tma_store_2d_hint(&dst_map, ring_base + s * a.tile_bytes, tc * a.tile_cols,
@@ -89,12 +93,17 @@ __global__ void __launch_bounds__(64, 1)
             ptx::bulk_commit_group();
             if (a.store_lag == 0) {
                 ptx::bulk_wait_group_read<0>();
+                trace_event(a.ctl, kRoleConsumer, nt, kEvReleased, i, s, 0);
                 ptx::mbar_arrive(ptx::smem_addr(empty + s));
             } else {
                 ptx::bulk_wait_group_read<1>();
-                if (i > 0) ptx::mbar_arrive(ptx::smem_addr(empty + (i - 1) % S));
+                if (i > 0) {
+                    trace_event(a.ctl, kRoleConsumer, nt, kEvReleased, i - 1, (i - 1) % S, 0);
+                    ptx::mbar_arrive(ptx::smem_addr(empty + (i - 1) % S));
+                }
             }
         }
+        trace_count(a.ctl, kRoleConsumer, nt);
         ptx::bulk_wait_group<0>();
     }
     __syncwarp();
