@@ -297,6 +297,14 @@ def measure_workloads(gbr, peaks, sm_mhz=None, steps=20, warmup=3):
             "value": round(v, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
             "roofline": {"bound": "alu", "achieved": round(v, 2), "peak": round(fp32_alu_peak, 1),
                          "unit": "TFLOP/s", "frac": round(v / fp32_alu_peak, 4)}}
+    # The historical producer: the same ring and consumers, fed by a cp.async
+    # warpgroup instead of one TMA lane.
+    for S in (2, 4):
+        v, ms = timed(lambda: gbr.gemm_bias_relu(dA, dB, db, dC, dtype="ffma_cpasync", stages=S), f)
+        out["gemm_fp32_4096_ffma_cpasync_S%d" % S] = {
+            "value": round(v, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
+            "roofline": {"bound": "alu", "achieved": round(v, 2), "peak": round(fp32_alu_peak, 1),
+                         "unit": "TFLOP/s", "frac": round(v / fp32_alu_peak, 4)}}
     del dA, dB, db, dC
     A, B, bias = inputs.workload("gemm_small")
     dA, dB, db = A.cuda(), B.cuda(), bias.cuda()

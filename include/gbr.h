@@ -45,11 +45,16 @@ typedef enum {
     GBR_F32_FFMA = 0,     /* fp32 in/out, strict fp32 FMA on CUDA cores        */
     GBR_F32_TF32 = 1,     /* fp32 in/out, TF32 tensor-core multiply, fp32 acc   */
     GBR_BF16 = 2,         /* bf16 A/B/C, fp32 bias, fp32 accumulation in TMEM   */
-    GBR_F32_FFMA_SYNC = 3 /* GBR_F32_FFMA computed by the homogeneous loop of
+    GBR_F32_FFMA_SYNC = 3, /* GBR_F32_FFMA computed by the homogeneous loop of
                              "pwwt.cn news/4436243" section 1.1 (all threads
                              load, sync, compute, sync; no roles, no ring):
                              the baseline the pipeline is measured against.
                              stages must be 1.                                 */
+    GBR_F32_FFMA_CPASYNC = 4 /* GBR_F32_FFMA with the historical producer: the
+                             producer warpgroup fills each ring stage with
+                             16-byte cp.async copies and arrives on full[s]
+                             with cp.async.mbarrier.arrive, instead of one TMA
+                             lane.  Same consumers, ring and results.          */
 } gbr_dtype;
 
 typedef enum {
@@ -207,7 +212,9 @@ int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage);
  * bias + ReLU epilogue.  Scratch (per call, stream-ordered, zeroed on the
  * stream, from a memory pool the library keeps per device): (T mod U) x tile
  * rows x 256 x 4 bytes plus counters.  Results differ from the unsplit kernel
- * only by the order of fp32 additions.
+ * only by the order of fp32 additions; that order follows the arrival of the
+ * parts, so a split tile can differ in its last bits from run to run (mode 0
+ * makes every launch deterministic).
  *   mode -1: auto (split when the last round shrinks by >= 1/8 of a tile),
  *         0: never, 1: whenever some tile can be split.
  * GBR_ERR_INVALID for other values.  The failure-detection self tests and

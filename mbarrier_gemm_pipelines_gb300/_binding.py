@@ -13,8 +13,9 @@ import threading
 from . import _build
 
 # gbr_dtype
-F32_FFMA, F32_TF32, BF16, F32_FFMA_SYNC = 0, 1, 2, 3
-DTYPE_NAMES = {"ffma": F32_FFMA, "tf32": F32_TF32, "bf16": BF16, "ffma_sync": F32_FFMA_SYNC}
+F32_FFMA, F32_TF32, BF16, F32_FFMA_SYNC, F32_FFMA_CPASYNC = 0, 1, 2, 3, 4
+DTYPE_NAMES = {"ffma": F32_FFMA, "tf32": F32_TF32, "bf16": BF16, "ffma_sync": F32_FFMA_SYNC,
+               "ffma_cpasync": F32_FFMA_CPASYNC}
 # gbr_status
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_ALIGN, ERR_SMEM, ERR_CUDA, ERR_TIMEOUT = range(7)
 STATUS_NAMES = {0: "GBR_OK", 1: "GBR_ERR_INVALID", 2: "GBR_ERR_UNSUPPORTED", 3: "GBR_ERR_ALIGN",

@@ -269,8 +269,9 @@ int choose_k_sub(int pair, int stages, int smem_optin) {
 // Largest ring depth for the dtype (tcgen05: that of the CTA-pair kernel).
 int gemm_max_stages(int dtype, int smem_optin) {
     if (dtype == GBR_F32_FFMA_SYNC) return 1;   // single-buffered by definition
-    return dtype == GBR_F32_FFMA ? max_stages_for(ffma_bytes_fn, smem_optin)
-                                 : umma_max_stages(2, smem_optin);
+    return dtype == GBR_F32_FFMA || dtype == GBR_F32_FFMA_CPASYNC
+               ? max_stages_for(ffma_bytes_fn, smem_optin)
+               : umma_max_stages(2, smem_optin);
 }
 
 // One CTA or a CTA pair per tile: forced by gbr_gemm_tuning, else the pair
@@ -448,7 +449,7 @@ int gbr_max_stages(int op, int dtype, int tile_rows, int tile_cols) {
     int r = get_ctx(&c);
     if (r != GBR_OK) return -r;
     if (op == GBR_OP_GEMM) {
-        if (dtype < GBR_F32_FFMA || dtype > GBR_F32_FFMA_SYNC)
+        if (dtype < GBR_F32_FFMA || dtype > GBR_F32_FFMA_CPASYNC)
             return -fail(GBR_ERR_INVALID, "bad dtype %d", dtype);
         return gemm_max_stages(dtype, c->smem_optin);
     }
@@ -490,8 +491,8 @@ int gbr_device_status(gbr_stream_t stream) {
 int gbr_selftest_gemm_skip_load(const void* A, const void* B, const float* bias, void* C,
                                 int64_t M, int64_t N, int64_t K, int dtype, int stages, int cta,
                                 int item, uint64_t limit_ns, gbr_stream_t stream) {
-    if (dtype == GBR_F32_FFMA_SYNC)
-        return fail(GBR_ERR_UNSUPPORTED, "self test: the homogeneous loop has no ring to break");
+    if (dtype == GBR_F32_FFMA_SYNC || dtype == GBR_F32_FFMA_CPASYNC)
+        return fail(GBR_ERR_UNSUPPORTED, "self test: runs on the TMA-fed rings only");
     return with_injection(cta, item, limit_ns, [&] {
         return gemm_bias_relu(A, B, bias, C, M, N, K, dtype, stages, stream);
     });
@@ -597,7 +598,7 @@ int staged_copy(const void* src, void* dst, int64_t rows, int64_t cols, int tile
 
 int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int64_t M, int64_t N,
                    int64_t K, int dtype, int stages, gbr_stream_t stream) {
-    if (dtype < GBR_F32_FFMA || dtype > GBR_F32_FFMA_SYNC)
+    if (dtype < GBR_F32_FFMA || dtype > GBR_F32_FFMA_CPASYNC)
         return fail(GBR_ERR_INVALID, "gemm_bias_relu: unknown dtype %d", dtype);
     const int64_t lim = int64_t(1) << 31;
     if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim)
@@ -652,7 +653,9 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
         return GBR_OK;
     }
 
-    if (dtype == GBR_F32_FFMA) {
+    if (dtype == GBR_F32_FFMA || dtype == GBR_F32_FFMA_CPASYNC) {
+        s.A = A;
+        s.B = B;
         s.m_tiles = int32_t(cdiv(M, kFfmaBM));
         s.n_tiles = int32_t(cdiv(N, kFfmaBN));
         s.num_kb = int32_t(cdiv(K, kFfmaBK));
@@ -692,7 +695,8 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
         if (r != GBR_OK) return r;
         if (occ < 1) return fail(GBR_ERR_SMEM, "FFMA GEMM does not fit on an SM");
         const int grid = int(std::min<int64_t>(s.num_tiles, int64_t(c->sm_count) * occ));
-        if ((e = launch_gemm_ffma(ma, mb, s, grid, smem, st)) != cudaSuccess)
+        if ((e = launch_gemm_ffma(ma, mb, s, grid, smem, st, dtype == GBR_F32_FFMA_CPASYNC)) !=
+            cudaSuccess)
             return cuda_fail(e, "launching FFMA GEMM");
         ++g_launches;
         return GBR_OK;
@@ -915,7 +919,7 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
 // ------------------------------------------------------------ host buffers
 int gemm_bias_relu_host(const void* hA, const void* hB, const float* hbias, void* hC, int64_t M,
                         int64_t N, int64_t K, int dtype, int stages, gbr_stream_t stream) {
-    if (dtype < GBR_F32_FFMA || dtype > GBR_F32_FFMA_SYNC)
+    if (dtype < GBR_F32_FFMA || dtype > GBR_F32_FFMA_CPASYNC)
         return fail(GBR_ERR_INVALID, "gemm_bias_relu_host: unknown dtype %d", dtype);
     const int64_t lim = int64_t(1) << 31;
     if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim)

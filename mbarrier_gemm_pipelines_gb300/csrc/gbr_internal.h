@@ -68,6 +68,8 @@ struct GemmShape {
     int32_t group_m;
     const float* bias;
     void* C;                       // used by epilogues that store with st.global
+    const void* A;                 // read directly only by the cp.async producer variant
+    const void* B;
     KernelCtl ctl;
     uint32_t k_sub;                // tensor-core GEMM: 128-byte K slices per ring stage (1, 2)
     uint32_t l2_hint;              // tensor-core GEMM operand loads: 0 none, 1 A and B
@@ -96,7 +98,7 @@ cudaError_t ffma_prepare(size_t smem);
 cudaError_t ffma_occupancy(size_t smem, int* blocks_per_sm);
 cudaError_t ffma_check_registers(int* regs);
 cudaError_t launch_gemm_ffma(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmShape& s,
-                             int grid, size_t smem, cudaStream_t stream);
+                             int grid, size_t smem, cudaStream_t stream, bool cpasync = false);
 // Homogeneous baseline (every thread loads, syncs, computes, syncs); one CTA
 // per 128x128 tile, single-buffered, plain global loads.
 cudaError_t launch_gemm_ffma_sync(const float* A, const float* B, const GemmShape& s,

@@ -430,6 +430,23 @@ __device__ __forceinline__ void fma_f32x2(uint64_t& d, uint64_t a, uint64_t b) {
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
 }
 
+// 16-byte asynchronous copy global -> shared, L2 only; `src_bytes` < 16
+// zero-fills the rest (0: nothing is read).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed;
+// the arrival counts against the barrier's expected count (.noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Load with acquire semantics at GPU scope (pairs with a release or with a
 // fence before the writer's atomic).
 __device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t* addr) {

@@ -112,6 +112,13 @@ __device__ __forceinline__ void ffma_epilogue(const uint64_t (&acc)[8][4], const
     }
 }
 
+// CPASYNC = false: one TMA lane produces each stage (the default).
+// CPASYNC = true: the historical producer ("gpu_warp_specialization" and
+// "pwwt.cn news/4436243" section 2: Ampere cp.async): the whole producer
+// warpgroup copies the stage with 16-byte cp.async per thread into the same
+// swizzled layout, and each of its 128 threads arrives on full[s] with
+// cp.async.mbarrier.arrive.noinc once its own copies have landed.
+template <bool CPASYNC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_ffma_kernel(const __grid_constant__ CUtensorMap mapA,
                      const __grid_constant__ CUtensorMap mapB, const GemmShape p) {
@@ -125,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            ptx::mbar_init(ptx::smem_addr(full + s), 1);
+            ptx::mbar_init(ptx::smem_addr(full + s), CPASYNC ? 128u : 1u);
             ptx::mbar_init(ptx::smem_addr(empty + s), kConsumerWarps);
         }
         *abort_flag = 0;
@@ -140,7 +147,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < 4) {
         ptx::setmaxnreg_dec<kProducerRegs>();
-        if (warp == 0 && lane == 0) {
+        if (CPASYNC) {
+            // ------------------------------------ cp.async producer warpgroup
+            const uint32_t pt = threadIdx.x;   // 0..127
+            const float* A = static_cast<const float*>(p.A);
+            const float* B = static_cast<const float*>(p.B);
+            uint32_t i = 0, ntr = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                uint32_t mt, nt;
+                raster_tile(t, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+                const int m0 = int(mt) * kFfmaBM, n0 = int(nt) * kFfmaBN;
+                for (int kb = 0; kb < p.num_kb; ++kb, ++i) {
+                    const uint32_t s = i % S, ph = (i / S) & 1u;
+                    if (!mbar_wait_warp(ptx::smem_addr(empty + s), ph ^ 1u, p.ctl, abort_flag,
+                                        kSiteProducerEmpty, i)) {
+                        ok = false;
+                        break;
+                    }
+                    if (pt == 0) {   // thread 0 traces for the warpgroup
+                        trace_event(p.ctl, kRoleProducer, ntr, kEvWaitDone, i, s, ph ^ 1u);
+                        trace_event(p.ctl, kRoleProducer, ntr, kEvIssued, i, s, 0);
+                    }
+                    const uint32_t st = ring_base + s * kFfmaStageBytes;
+                    const int k0 = kb * kFfmaBK;
+#pragma unroll
+                    for (uint32_t j = 0; j < 8; ++j) {   // A: 128 rows x 8 chunks of 16 B
+                        const uint32_t c = pt + 128u * j, row = c >> 3, k4 = c & 7u;
+                        const int m = m0 + int(row), k = k0 + int(4 * k4);
+                        const bool in = m < p.M && k < p.K;
+                        ptx::cp_async_16(st + row * 128u + ((k4 ^ (row & 7u)) << 4),
+                                         in ? A + size_t(m) * p.K + k : A, in ? 16u : 0u);
+                    }
+#pragma unroll
+                    for (uint32_t j = 0; j < 8; ++j) {   // B: 32 K rows x 32 chunks of 16 B
+                        const uint32_t c = pt + 128u * j, kr = c >> 5, n4 = c & 31u;
+                        const int k = k0 + int(kr), n = n0 + int(4 * n4);
+                        const bool in = k < p.K && n < p.N;
+                        ptx::cp_async_16(st + kABytes + (n4 >> 3) * kBPanelBytes + kr * 128u +
+                                             (((n4 & 7u) ^ (kr & 7u)) << 4),
+                                         in ? B + size_t(k) * p.N + n : B, in ? 16u : 0u);
+                    }
+                    ptx::cp_async_mbar_arrive_noinc(ptx::smem_addr(full + s));
+                }
+            }
+            if (pt == 0) trace_count(p.ctl, kRoleProducer, ntr);
+            ptx::cp_async_wait_all();   // no copy may still be writing when the CTA exits
+        } else if (warp == 0 && lane == 0) {
             // ------------------------------------------------ producer
             uint32_t i = 0, ntr = 0;
             bool ok = true;
@@ -291,34 +344,44 @@ size_t ffma_smem_bytes(int stages) {
 
 cudaError_t ffma_prepare(size_t smem) {
     static std::mutex mu;
-    static size_t set[kMaxDeviceSlots] = {};
+    static size_t set[kMaxDeviceSlots][2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDeviceSlots) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(mu);
-    return raise_smem_limit(reinterpret_cast<const void*>(gemm_ffma_kernel), smem, &set[dev]);
+    if ((e = raise_smem_limit(reinterpret_cast<const void*>(gemm_ffma_kernel<false>), smem,
+                              &set[dev][0])) != cudaSuccess)
+        return e;
+    return raise_smem_limit(reinterpret_cast<const void*>(gemm_ffma_kernel<true>), smem, &set[dev][1]);
 }
 
 cudaError_t ffma_occupancy(size_t smem, int* blocks_per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, gemm_ffma_kernel,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, gemm_ffma_kernel<false>,
                                                          kThreads, smem);
 }
 
 // The register split must fit in what the CTA is launched with, or the
 // consumers' setmaxnreg.inc would wait forever for registers.
 cudaError_t ffma_check_registers(int* regs) {
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, gemm_ffma_kernel);
-    if (e != cudaSuccess) return e;
-    *regs = fa.numRegs;
     const long need = 128L * kProducerRegs + 256L * kConsumerRegs;
-    return (long(fa.numRegs) * kThreads >= need) ? cudaSuccess : cudaErrorInvalidConfiguration;
+    for (const void* fn : {reinterpret_cast<const void*>(gemm_ffma_kernel<false>),
+                           reinterpret_cast<const void*>(gemm_ffma_kernel<true>)}) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+        if (e != cudaSuccess) return e;
+        *regs = fa.numRegs;
+        if (long(fa.numRegs) * kThreads < need) return cudaErrorInvalidConfiguration;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_gemm_ffma(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmShape& s,
-                             int grid, size_t smem, cudaStream_t stream) {
-    gemm_ffma_kernel<<<grid, kThreads, smem, stream>>>(mapA, mapB, s);
+                             int grid, size_t smem, cudaStream_t stream, bool cpasync) {
+    if (cpasync)
+        gemm_ffma_kernel<true><<<grid, kThreads, smem, stream>>>(mapA, mapB, s);
+    else
+        gemm_ffma_kernel<false><<<grid, kThreads, smem, stream>>>(mapA, mapB, s);
     return cudaGetLastError();
 }
 

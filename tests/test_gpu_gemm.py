@@ -52,7 +52,7 @@ SHAPES = [(128, 128, 32), (256, 512, 256), (200, 136, 104), (129, 264, 40), (1, 
           (300, 520, 200), (640, 384, 1000), (383, 776, 1352)]
 
 
-VARIANTS = [("ffma", -1), ("tf32", 1), ("tf32", 2), ("bf16", 1), ("bf16", 2)]
+VARIANTS = [("ffma", -1), ("ffma_cpasync", -1), ("tf32", 1), ("tf32", 2), ("bf16", 1), ("bf16", 2)]
 
 
 @pytest.mark.parametrize("dtype,pair", VARIANTS)
@@ -75,7 +75,7 @@ def test_stage_sweep(gbr, dtype, pair, ks):
     A, B, bias = inputs.gemm_normal(M, N, K, seed=5)
     if dtype == "bf16":
         A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
-    smax = gbr.max_stages(gbr.OP_GEMM, {"ffma": 0, "tf32": 1, "bf16": 2}[dtype])
+    smax = gbr.max_stages(gbr.OP_GEMM, {"ffma": 0, "ffma_cpasync": 4, "tf32": 1, "bf16": 2}[dtype])
     assert smax >= 4
     if pair == 1:
         smax = 4                                   # one CTA per tile holds 4 stages
@@ -234,8 +234,8 @@ def _sampled(gbr, A, B, bias, dtype, stages, npts, seed):
     return C
 
 
-@pytest.mark.parametrize("dtype,S,pair", [("ffma", 3, -1), ("ffma", 4, -1), ("tf32", 3, -1),
-                                           ("tf32", 4, -1), ("tf32", 4, 1)])
+@pytest.mark.parametrize("dtype,S,pair", [("ffma", 3, -1), ("ffma", 4, -1), ("ffma_cpasync", 4, -1),
+                                           ("tf32", 3, -1), ("tf32", 4, -1), ("tf32", 4, 1)])
 def test_config3_fp32_4096(gbr, dtype, S, pair):
     A, B, bias = inputs.workload("gemm_fp32")
     with tuned(gbr, pair):

@@ -38,14 +38,15 @@ def test_copy_trace(gbr, S, lag):
     assert errs == [], errs[:5]
 
 
+@pytest.mark.parametrize("dtype", ["ffma", "ffma_cpasync"])
 @pytest.mark.parametrize("S", [1, 2, 3, 4])
-def test_ffma_trace(gbr, S):
+def test_ffma_trace(gbr, dtype, S):
     A, B, bias = inputs.gemm_normal(512, 512, 1024, seed=31)   # 16 tiles x 32 k-blocks
     with trace.Recorder(cap=256) as rec:
-        C = gbr.gemm_bias_relu(A.cuda(), B.cuda(), bias.cuda(), dtype="ffma", stages=S)
+        C = gbr.gemm_bias_relu(A.cuda(), B.cuda(), bias.cuda(), dtype=dtype, stages=S)
         ev, cnt = rec.events()
     gbr.check_device()
-    assert rel_frobenius(to_host_f64(C), oracle.gemm_bias_relu(A, B, bias)) <= TOL["ffma"]
+    assert rel_frobenius(to_host_f64(C), oracle.gemm_bias_relu(A, B, bias)) <= TOL[dtype]
     errs = check(ev, cnt, S)
     assert errs == [], errs[:5]
 
