@@ -323,6 +323,23 @@ def measure_workloads(gbr, peaks, sm_mhz=None, steps=20, warmup=3):
         "value": round(v, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4), "counts": counts,
         "roofline": {"bound": "tensor", "achieved": round(v, 2), "peak": bf16_peak,
                      "unit": "TFLOP/s", "frac": round(v / bf16_peak, 4)}}
+    del dX, dW, db, dC
+    # Skewed expert sizes (halving from 2048 rows): tiles of the small experts
+    # stream their whole weight matrix for few rows, so tiles differ in cost.
+    # Static tile order versus tiles taken from an atomic counter.
+    counts = [2048, 1024, 512, 256, 128, 64, 32, 32]
+    _, X, W, b = inputs.grouped(tokens=sum(counts), experts=8, K=4096, N=14336, seed=4)
+    dX, dW, db = X.cuda(), W.cuda(), b.cuda()
+    dC = torch.empty((sum(counts), W.shape[2]), dtype=torch.bfloat16, device="cuda")
+    f = 2.0 * sum(counts) * W.shape[1] * W.shape[2]
+    for label, dyn in (("static", False), ("dynamic", True)):
+        gbr.gemm_dynamic_schedule(dyn)
+        v, ms = timed(lambda: gbr.gemm_bias_relu_grouped(dX, dW, db, counts, dC, stages=3), f)
+        out["grouped_bf16_moe_skewed_%s_S3" % label] = {
+            "value": round(v, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4), "counts": counts,
+            "roofline": {"bound": "tensor", "achieved": round(v, 2), "peak": bf16_peak,
+                         "unit": "TFLOP/s", "frac": round(v / bf16_peak, 4)}}
+    gbr.gemm_dynamic_schedule(False)
     return out
 
 

@@ -223,6 +223,20 @@ int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage);
 int gbr_gemm_split_tail(int mode);
 
 /*
+ * Dynamic tile order of the tensor-core GEMMs (dense and grouped), for all
+ * later calls in the process.  on = 0 (default): each persistent unit runs
+ * tiles unit, unit + units, ... (with the split tail above).  on = 1: the
+ * even CTA's producer of each unit takes the next tile from a global atomic
+ * counter (a zeroed word from the library's pool) and hands its id to the
+ * MMA lane, the epilogue warps and the odd CTA's producer through a 4-slot
+ * ring of tile ids in shared memory, guarded by its own full/empty
+ * mbarriers; units that finish early take more tiles.  The split tail is off
+ * in this mode.  Results equal the static order's bit for bit (every tile
+ * adds the same products in the same order).  GBR_ERR_INVALID for other values.
+ */
+int gbr_gemm_dynamic_schedule(int on);
+
+/*
  * gemm_bias_relu_host -- gemm_bias_relu on HOST buffers: copies A, B and bias
  * to the device, computes, and copies C back, overlapping the three.  The
  * device buffers come from the library's stream-ordered pool.  M is cut into

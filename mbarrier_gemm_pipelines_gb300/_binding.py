@@ -38,6 +38,7 @@ SIGNATURES = {
     "gbr_copy_tuning": (_i32, [_i32, _i32, _i32]),
     "gbr_gemm_tuning": (_i32, [_i32, _i32, _i32, _i32]),
     "gbr_gemm_split_tail": (_i32, [_i32]),
+    "gbr_gemm_dynamic_schedule": (_i32, [_i32]),
     "gbr_trace_buffer": (_i32, [_vp, _u64]),
     "gbr_selftest_wait_timeout": (_i32, [_u64, _vp]),
     "gbr_selftest_gemm_skip_load": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32,
@@ -250,6 +251,11 @@ def gemm_split_tail(mode: int = -1) -> None:
     """Split the last round of tensor-core GEMM tiles along K: -1 auto, 0 never,
     1 whenever possible (see gbr.h)."""
     check(lib().gbr_gemm_split_tail(int(mode)))
+
+
+def gemm_dynamic_schedule(on: bool) -> None:
+    """Tensor-core GEMM tiles from an atomic counter (True) or the static order (see gbr.h)."""
+    check(lib().gbr_gemm_dynamic_schedule(int(bool(on))))
 
 
 def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:

@@ -36,6 +36,7 @@ int g_gemm_group_m = -1;   // -1 auto: tile rows per raster band
 int g_gemm_l2_hint = -1;   // -1 auto (none): L2 policy of the operand loads
 int g_gemm_k_sub = -1;     // -1 auto (1): 128-byte K slices per ring stage
 int g_gemm_split = -1;     // -1 auto, 0 off, 1 on whenever some tile can be split
+int g_gemm_dynamic = 0;    // 1: tensor-core GEMMs take tiles from an atomic counter
 uint8_t* g_trace = nullptr;  // event trace buffer (device memory of the caller), or null
 uint32_t g_trace_cap = 0;    // records per (CTA, role)
 
@@ -312,6 +313,27 @@ size_t plan_split(GemmShape& s, int64_t units, SplitScratch kind) {
     return plan_split_fields(s, units, mode) ? split_scratch_bytes(s, kind) : 0;
 }
 
+// Dynamic tile order (the split tail is then off): requested, and usable?
+bool dynamic_wanted(const GemmShape& s) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_gemm_dynamic != 0 && !s.inject.enabled && s.num_tiles > 0;
+}
+
+// Its zeroed counter, from the device's pool (*ws null when not wanted).
+int dynamic_scratch(const DevCtx& c, GemmShape& s, cudaStream_t st, void** ws) {
+    *ws = nullptr;
+    if (!dynamic_wanted(s)) return GBR_OK;
+    cudaError_t e = cudaMallocFromPoolAsync(ws, 256, c.pool, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync(tile counter)");
+    if ((e = cudaMemsetAsync(*ws, 0, sizeof(uint32_t), st)) != cudaSuccess) {
+        cudaFreeAsync(*ws, st);
+        *ws = nullptr;
+        return cuda_fail(e, "cudaMemsetAsync(tile counter)");
+    }
+    s.dyn_counter = static_cast<uint32_t*>(*ws);
+    return GBR_OK;
+}
+
 // Scratch of one split launch from the device's pool, zeroed on the stream:
 // the counters, then the tiles' sums.
 int split_scratch(const DevCtx& c, GemmShape& s, SplitScratch kind, size_t bytes, cudaStream_t st,
@@ -415,6 +437,14 @@ int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage) {
     g_gemm_group_m = group_m;
     g_gemm_l2_hint = l2_hint;
     g_gemm_k_sub = k_per_stage;
+    return GBR_OK;
+}
+
+int gbr_gemm_dynamic_schedule(int on) {
+    if (on != 0 && on != 1)
+        return fail(GBR_ERR_INVALID, "gbr_gemm_dynamic_schedule: on must be 0 or 1");
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_gemm_dynamic = on;
     return GBR_OK;
 }
 
@@ -732,7 +762,8 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
     if ((e = umma_prepare(kind, false, pair, smem)) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(tcgen05 GEMM)");
     const int64_t units = c->sm_count / pair;
-    const size_t split_bytes = plan_split(s, units, umma_split_scratch(pair));
+    const size_t split_bytes =
+        dynamic_wanted(s) ? 0 : plan_split(s, units, umma_split_scratch(pair));
     const int grid = pair * int(split_bytes ? units : std::min<int64_t>(s.num_tiles, units));
     float* bt = nullptr;  // TF32 only: K-major copy of B, stream-ordered scratch
     if (K > 0) {
@@ -765,12 +796,16 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
         mb = mc;
     }
     void* ws = nullptr;
-    if ((r = split_scratch(*c, s, umma_split_scratch(pair), split_bytes, st, &ws)) != GBR_OK) {
+    void* dyn_ws = nullptr;
+    if ((r = split_scratch(*c, s, umma_split_scratch(pair), split_bytes, st, &ws)) != GBR_OK ||
+        (r = dynamic_scratch(*c, s, st, &dyn_ws)) != GBR_OK) {
+        if (ws) cudaFreeAsync(ws, st);
         if (bt) cudaFreeAsync(bt, st);
         return r;
     }
     e = launch_gemm_umma(kind, pair, ma, mb, mc, s, grid, smem, st);
     if (ws) cudaFreeAsync(ws, st);
+    if (dyn_ws) cudaFreeAsync(dyn_ws, st);
     if (bt) cudaFreeAsync(bt, st);
     if (e != cudaSuccess) return cuda_fail(e, "launching tcgen05 GEMM");
     ++g_launches;
@@ -904,13 +939,20 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
     cudaError_t e = umma_prepare(kUmmaBf16, true, pair, smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(grouped GEMM)");
     const int64_t units = c->sm_count / pair;
-    const size_t split_bytes = plan_split(s, units, umma_split_scratch(pair));
+    const size_t split_bytes =
+        dynamic_wanted(s) ? 0 : plan_split(s, units, umma_split_scratch(pair));
     const int grid = pair * int(split_bytes ? units : std::min<int64_t>(s.num_tiles, units));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void* ws = nullptr;
-    if ((r = split_scratch(*c, s, umma_split_scratch(pair), split_bytes, st, &ws)) != GBR_OK) return r;
+    void* dyn_ws = nullptr;
+    if ((r = split_scratch(*c, s, umma_split_scratch(pair), split_bytes, st, &ws)) != GBR_OK ||
+        (r = dynamic_scratch(*c, s, st, &dyn_ws)) != GBR_OK) {
+        if (ws) cudaFreeAsync(ws, st);
+        return r;
+    }
     e = launch_gemm_umma_grouped(pair, mx, mw, mc, g, s, int64_t(N), grid, smem, st);
     if (ws) cudaFreeAsync(ws, st);
+    if (dyn_ws) cudaFreeAsync(dyn_ws, st);
     if (e != cudaSuccess) return cuda_fail(e, "launching grouped GEMM");
     ++g_launches;
     return GBR_OK;

@@ -16,12 +16,15 @@ constexpr uint32_t kDevErrTimeout = 1u;
 enum WaitSite : uint32_t {
     kSiteProducerEmpty = 0x11,
     kSiteProducerDrain = 0x12,
+    kSiteProducerTile = 0x13,
     kSiteConsumerFull = 0x21,
     kSiteMmaFull = 0x31,
     kSiteMmaAccEmpty = 0x32,
     kSiteMmaDrain = 0x33,
+    kSiteMmaTile = 0x34,
     kSiteEpiAccFull = 0x41,
     kSiteEpiSplitSum = 0x42,
+    kSiteEpiTile = 0x43,
     kSiteStorerFull = 0x51,
     kSiteSelfTest = 0x71,
 };

@@ -88,6 +88,11 @@ struct GemmShape {
     int32_t sk_iters;
     float* sk_sum;                 // [sk_tiles][tile rows][256] fp32, zeroed
     uint32_t* sk_count;            // [sk_tiles][CTAs per tile][4 epilogue warps][2], zeroed
+    // Dynamic tile order (tensor-core GEMM; null: the static order above).
+    // The even CTA's producer takes the next tile from this zeroed counter
+    // with atomicAdd and hands its id to every role through a shared-memory
+    // ring; no split tail then.
+    uint32_t* dyn_counter;
 };
 
 // FFMA path (strict fp32, CUDA cores): 128x128x32 tiles.

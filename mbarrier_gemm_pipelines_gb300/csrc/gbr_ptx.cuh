@@ -303,6 +303,11 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 // Arrive on an mbarrier that may live in another CTA of the cluster.
+// 32-bit store to shared memory of a CTA of the cluster (mapa address).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");

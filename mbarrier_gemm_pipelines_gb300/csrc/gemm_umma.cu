@@ -218,6 +218,84 @@ __device__ __forceinline__ void sum_accum32(const float4* blk, uint32_t c, uint3
     }
 }
 
+// Dynamic tile order: a ring of kTileRing tile ids in shared memory.  The
+// even CTA's producer (the fetcher) takes tile ids from the global counter
+// in order of request and publishes item j's id in slot j % kTileRing of both
+// CTAs; every other role reads it there and arrives on the even CTA's
+// tile_empty[slot] when done.  kTileEnd marks the end of the work.
+constexpr uint32_t kTileRing = 4;
+constexpr uint32_t kTileEnd = 0xFFFFFFFFu;
+
+struct TileRing {
+    uint64_t* full;    // [kTileRing], 1 arrival (the fetcher)
+    uint64_t* empty;   // [kTileRing], one arrival per reader
+    uint32_t* ids;     // [kTileRing]
+};
+
+__device__ __forceinline__ void whole_tile(const GemmShape& s, uint32_t t, WorkItem& w) {
+    w.tile = t;
+    w.kb0 = 0;
+    w.kb1 = s.num_kb;
+    w.part = 0;
+    w.parts = 1;
+    w.sk = 0;
+}
+
+// Fetcher: item j of this unit.  The fetcher runs kTileAhead items ahead of
+// its own use, so that the atomic's round trip is not on the path from one
+// tile's loads to the next: before item j it has taken items up to
+// j + kTileAhead (fetched counts them; done once it published the end).
+// False at the end or when a wait gave up.
+constexpr uint32_t kTileAhead = kTileRing - 2;
+
+template <int PAIR>
+__device__ __forceinline__ bool dyn_fetch(const GemmShape& s, const TileRing& r, uint32_t j,
+                                          volatile int* abort_flag, uint32_t& fetched, bool& done,
+                                          WorkItem& w) {
+    while (!done && fetched <= j + kTileAhead) {
+        const uint32_t i = fetched, slot = i % kTileRing, ph = (i / kTileRing) & 1u;
+        if (!mbar_wait<PAIR == 2>(ptx::smem_addr(r.empty + slot), ph ^ 1u, s.ctl, abort_flag,
+                                  kSiteProducerTile, i))
+            return false;
+        uint32_t t = atomicAdd(s.dyn_counter, 1u);
+        if (t >= uint32_t(s.num_tiles)) t = kTileEnd;
+        r.ids[slot] = t;
+        if (PAIR == 2) {
+            ptx::st_shared_cluster_u32(ptx::mapa_shared(ptx::smem_addr(r.ids + slot), 1), t);
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_addr(r.full + slot), 1));
+        }
+        ptx::mbar_arrive(ptx::smem_addr(r.full + slot));
+        done = t == kTileEnd;
+        ++fetched;
+    }
+    const uint32_t t = r.ids[j % kTileRing];   // written by this thread above
+    whole_tile(s, t, w);
+    return t != kTileEnd;
+}
+
+// Reader (one thread, or a whole warp with warp = true): item j's tile id.
+template <int PAIR, bool WARP>
+__device__ __forceinline__ bool dyn_read(const GemmShape& s, const TileRing& r, uint32_t j,
+                                         uint32_t lane, volatile int* abort_flag, uint32_t site,
+                                         WorkItem& w) {
+    const uint32_t slot = j % kTileRing, ph = (j / kTileRing) & 1u;
+    const uint32_t fb = ptx::smem_addr(r.full + slot);
+    const bool ok = WARP ? mbar_wait_warp<PAIR == 2>(fb, ph, s.ctl, abort_flag, site, j)
+                         : mbar_wait<PAIR == 2>(fb, ph, s.ctl, abort_flag, site, j);
+    if (!ok) return false;
+    const uint32_t t = *reinterpret_cast<volatile uint32_t*>(r.ids + slot);
+    if (WARP) __syncwarp();
+    if (!WARP || lane == 0) {
+        const uint32_t eb = ptx::smem_addr(r.empty + slot);
+        if (PAIR == 2)
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(eb, 0));
+        else
+            ptx::mbar_arrive(eb);
+    }
+    whole_tile(s, t, w);
+    return t != kTileEnd;
+}
+
 // The epilogue warp is done reading accumulator buffer `ae` belongs to.
 template <int PAIR>
 __device__ __forceinline__ void acc_release(uint32_t ae, uint32_t lane) {
@@ -231,9 +309,14 @@ __device__ __forceinline__ void acc_release(uint32_t ae, uint32_t lane) {
     }
 }
 
-template <int KIND, bool GROUPED, int PAIR, int KSUB, bool TRACE>
+// MODE 0: the static tile order only (the instances the library normally runs).
+// MODE 1: event trace points, and the dynamic order when requested.
+// MODE 2: the dynamic tile order, without trace points.
+template <int KIND, bool GROUPED, int PAIR, int KSUB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_umma_kernel(const __grid_constant__ UmmaParams<GROUPED> P) {
+    constexpr bool kTrace = MODE == 1;
+    constexpr bool kDyn = MODE != 0;
     using K_ = Kind<KIND>;
     using PR = Pair<PAIR>;
     constexpr bool kCl = PAIR == 2;                      // cluster-scope waits
@@ -255,6 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    TileRing tiles;
+    tiles.full = drain + 2;
+    tiles.empty = tiles.full + kTileRing;
+    tiles.ids = reinterpret_cast<uint32_t*>(tiles.empty + kTileRing);
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const uint32_t rank = PAIR == 2 ? ptx::cluster_ctarank() : 0u;
@@ -271,6 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(ptx::smem_addr(acc_empty + a), 4 * PAIR);        // epilogue warps
         }
         ptx::mbar_init(ptx::smem_addr(drain), 1);
+        for (uint32_t d = 0; d < kTileRing; ++d) {
+            ptx::mbar_init(ptx::smem_addr(tiles.full + d), 1);
+            // readers: the MMA lane, the epilogue warps of the unit, the odd CTA's producer
+            ptx::mbar_init(ptx::smem_addr(tiles.empty + d), 1 + 4 * PAIR + (PAIR == 2 ? 1 : 0));
+        }
         *abort_flag = 0;
         ptx::fence_barrier_init();
     } else if (threadIdx.x == 32) {
@@ -305,10 +397,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_normal = ptx::l2_policy_evict_normal();
             const uint64_t pol_a = s.l2_hint == 2 ? pol_first : s.l2_hint == 4 ? pol_normal : pol_last;
             const uint64_t pol_b = s.l2_hint == 3 ? pol_first : s.l2_hint == 4 ? pol_normal : pol_last;
-            uint32_t it = 0, ntr = 0;
-            bool ok = true;
+            uint32_t it = 0, ntr = 0, fetched = 0;
+            bool ok = true, fetch_done = false;
+            const bool dyn = kDyn && s.dyn_counter != nullptr;
             WorkItem w;
-            for (uint32_t j = 0; ok && work_item(s, unit, units, j, w); ++j) {
+            for (uint32_t j = 0;
+                 ok && (!dyn ? work_item(s, unit, units, j, w)
+                             : rank == 0 ? dyn_fetch<PAIR>(s, tiles, j, abort_flag, fetched,
+                                                           fetch_done, w)
+                                         : dyn_read<PAIR, false>(s, tiles, j, 0, abort_flag,
+                                                                  kSiteProducerTile, w));
+                 ++j) {
                 const TileInfo ti = decode_tile<GROUPED, PAIR>(P, w.tile, rank);
                 const int32_t bcol0 = ti.n0 + int32_t(rank * PR::b_cols);
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
@@ -318,12 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (TRACE) trace_event(s.ctl, kRoleProducer, ntr, kEvWaitDone, it, slot, ph ^ 1u);
+                    if (kTrace) trace_event(s.ctl, kRoleProducer, ntr, kEvWaitDone, it, slot, ph ^ 1u);
                     const uint32_t fb_local = ptx::smem_addr(full + slot);
                     const uint32_t fb = PAIR == 2 ? ptx::mapa_shared(fb_local, 0) : fb_local;
                     if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, PAIR * stage_bytes);
                     if (PAIR == 1 && inject_skip(s.inject, it)) continue;   // self test
-                    if (TRACE) trace_event(s.ctl, kRoleProducer, ntr, kEvIssued, it, slot, 0);
+                    if (kTrace) trace_event(s.ctl, kRoleProducer, ntr, kEvIssued, it, slot, 0);
                     const uint32_t stage_base = ring_base + slot * stage_bytes;
 #pragma unroll
                     for (uint32_t h = 0; h < ksub; ++h) {
@@ -349,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (TRACE) trace_count(s.ctl, kRoleProducer, ntr);
+            if (kTrace) trace_count(s.ctl, kRoleProducer, ntr);
             if (*abort_flag && rank == 0) {
                 const uint32_t n = it < uint32_t(S) ? it : uint32_t(S);
                 for (uint32_t j = it - n; j < it; ++j)
@@ -360,13 +459,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ring_base = ptx::smem_addr(ring);
             uint32_t it = 0, tl = 0, ntr = 0, nta = 0;
             bool ok = true;
+            const bool dyn = kDyn && s.dyn_counter != nullptr;
             WorkItem w;
-            for (; ok && work_item(s, unit, units, tl, w); ++tl) {
+            for (; ok && (!dyn ? work_item(s, unit, units, tl, w)
+                               : dyn_read<PAIR, false>(s, tiles, tl, 0, abort_flag, kSiteMmaTile, w));
+                 ++tl) {
                 const uint32_t a = tl & 1u, aph = (tl >> 1) & 1u;
                 if (!mbar_wait<kCl>(ptx::smem_addr(acc_empty + a), aph ^ 1u, s.ctl, abort_flag,
                                     kSiteMmaAccEmpty, tl))
                     break;
-                if (TRACE) trace_event(s.ctl, kRoleMmaAcc, nta, kEvWaitDone, tl, a, aph ^ 1u);
+                if (kTrace) trace_event(s.ctl, kRoleMmaAcc, nta, kEvWaitDone, tl, a, aph ^ 1u);
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + a * kAccCols;
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
@@ -376,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (TRACE) trace_event(s.ctl, kRoleConsumer, ntr, kEvWaitDone, it, slot, ph);
+                    if (kTrace) trace_event(s.ctl, kRoleConsumer, ntr, kEvWaitDone, it, slot, ph);
                     ptx::tc_fence_after_sync();
                     const uint32_t stage_base = ring_base + slot * stage_bytes;
 #pragma unroll
@@ -404,14 +506,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     }
-                    if (TRACE) trace_event(s.ctl, kRoleConsumer, ntr, kEvReleased, it, slot, 0);
+                    if (kTrace) trace_event(s.ctl, kRoleConsumer, ntr, kEvReleased, it, slot, 0);
                     if (PAIR == 2)
                         ptx::mma_commit_pair_multicast(ptx::smem_addr(empty + slot), 0x3);
                     else
                         ptx::mma_commit(ptx::smem_addr(empty + slot));
                 }
                 if (!ok) break;
-                if (TRACE) trace_event(s.ctl, kRoleMmaAcc, nta, kEvIssued, tl, a, 0);
+                if (kTrace) trace_event(s.ctl, kRoleMmaAcc, nta, kEvIssued, tl, a, 0);
                 if (w.kb1 > w.kb0) {
                     if (PAIR == 2)
                         ptx::mma_commit_pair_multicast(ptx::smem_addr(acc_full + a), 0x3);
@@ -427,8 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (TRACE) trace_count(s.ctl, kRoleConsumer, ntr);
-            if (TRACE) trace_count(s.ctl, kRoleMmaAcc, nta);
+            if (kTrace) trace_count(s.ctl, kRoleConsumer, ntr);
+            if (kTrace) trace_count(s.ctl, kRoleMmaAcc, nta);
             // No MMA may still be running when TMEM (or the peer's smem) is released.
             if (PAIR == 2)
                 ptx::mma_commit_pair_multicast(ptx::smem_addr(drain), 0x1);
@@ -445,9 +547,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t row_off = lane * 128u;
         const uint32_t swz = lane & 7u;
         uint32_t chunk_ctr = 0, ntr = 0;
-        const bool tracer = TRACE && q == 0 && lane == 0;   // one epilogue lane
+        const bool tracer = kTrace && s.ctl.trace != nullptr && q == 0 && lane == 0;   // one lane
+        const bool dyn = kDyn && s.dyn_counter != nullptr;
         WorkItem w;
-        for (uint32_t tl = 0; work_item(s, unit, units, tl, w); ++tl) {
+        for (uint32_t tl = 0;
+             !dyn ? work_item(s, unit, units, tl, w)
+                  : dyn_read<PAIR, true>(s, tiles, tl, lane, abort_flag, kSiteEpiTile, w);
+             ++tl) {
             const TileInfo ti = decode_tile<GROUPED, PAIR>(P, w.tile, rank);
             const uint32_t a = tl & 1u, aph = (tl >> 1) & 1u;
             const uint32_t ae = ptx::smem_addr(acc_empty + a);
@@ -595,34 +701,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int KIND, bool GROUPED, int PAIR, int KSUB, bool TRACE>
+template <int KIND, bool GROUPED, int PAIR, int KSUB, int MODE>
 void* kernel_ptr() {
-    return reinterpret_cast<void*>(&gemm_umma_kernel<KIND, GROUPED, PAIR, KSUB, TRACE>);
+    return reinterpret_cast<void*>(&gemm_umma_kernel<KIND, GROUPED, PAIR, KSUB, MODE>);
 }
 
-// Instances with the event trace compiled in run only while a trace buffer is
-// set: the trace points cost the untraced kernels ~2% on the MMA lane.
-template <int KIND, bool GROUPED, bool TRACE>
-void* select_kernel_kgt(int pair, int ksub) {
+// Mode 0 runs unless a trace buffer (mode 1) or the dynamic order (mode 2) is
+// requested: compiled into the plain instances, that code costs them 2-5%
+// (trace points and per-item tile reads on the MMA lane, register pressure in
+// the epilogue).
+template <int KIND, bool GROUPED, int MODE>
+void* select_kernel_kgm(int pair, int ksub) {
     if (pair == 2)
-        return ksub == 2 ? kernel_ptr<KIND, GROUPED, 2, 2, TRACE>()
-                         : kernel_ptr<KIND, GROUPED, 2, 1, TRACE>();
-    return ksub == 2 ? kernel_ptr<KIND, GROUPED, 1, 2, TRACE>()
-                     : kernel_ptr<KIND, GROUPED, 1, 1, TRACE>();
+        return ksub == 2 ? kernel_ptr<KIND, GROUPED, 2, 2, MODE>()
+                         : kernel_ptr<KIND, GROUPED, 2, 1, MODE>();
+    return ksub == 2 ? kernel_ptr<KIND, GROUPED, 1, 2, MODE>()
+                     : kernel_ptr<KIND, GROUPED, 1, 1, MODE>();
 }
 
 template <int KIND, bool GROUPED>
-void* select_kernel_kg(int pair, int ksub, bool trace) {
-    return trace ? select_kernel_kgt<KIND, GROUPED, true>(pair, ksub)
-                 : select_kernel_kgt<KIND, GROUPED, false>(pair, ksub);
+void* select_kernel_kg(int pair, int ksub, int mode) {
+    return mode == 1 ? select_kernel_kgm<KIND, GROUPED, 1>(pair, ksub)
+         : mode == 2 ? select_kernel_kgm<KIND, GROUPED, 2>(pair, ksub)
+                     : select_kernel_kgm<KIND, GROUPED, 0>(pair, ksub);
 }
 
-void* select_kernel(int kind, bool grouped, int pair, int ksub, bool trace) {
+void* select_kernel(int kind, bool grouped, int pair, int ksub, int mode) {
     if (kind == kUmmaBf16)
-        return grouped ? select_kernel_kg<kUmmaBf16, true>(pair, ksub, trace)
-                       : select_kernel_kg<kUmmaBf16, false>(pair, ksub, trace);
-    return grouped ? select_kernel_kg<kUmmaTf32, true>(pair, ksub, trace)
-                   : select_kernel_kg<kUmmaTf32, false>(pair, ksub, trace);
+        return grouped ? select_kernel_kg<kUmmaBf16, true>(pair, ksub, mode)
+                       : select_kernel_kg<kUmmaBf16, false>(pair, ksub, mode);
+    return grouped ? select_kernel_kg<kUmmaTf32, true>(pair, ksub, mode)
+                   : select_kernel_kg<kUmmaTf32, false>(pair, ksub, mode);
 }
 
 int ksub_of(const GemmShape& s) { return s.k_sub == 2 ? 2 : 1; }
@@ -645,8 +754,8 @@ cudaError_t launch_umma(int kind, int pair, const UmmaParams<GROUPED>& P, int gr
     cfg.attrs = attr;
     cfg.numAttrs = pair == 2 ? 1 : 0;
     void* args[] = {const_cast<UmmaParams<GROUPED>*>(&P)};
-    return cudaLaunchKernelExC(
-        &cfg, select_kernel(kind, GROUPED, pair, ksub_of(P.s), P.s.ctl.trace != nullptr), args);
+    const int mode = P.s.ctl.trace != nullptr ? 1 : P.s.dyn_counter != nullptr ? 2 : 0;
+    return cudaLaunchKernelExC(&cfg, select_kernel(kind, GROUPED, pair, ksub_of(P.s), mode), args);
 }
 
 }  // namespace
@@ -667,17 +776,17 @@ size_t umma_smem_bytes(int stages) { return umma_smem_bytes(stages, 1); }
 
 cudaError_t umma_prepare(int kind, bool grouped, int pair, size_t smem) {
     static std::mutex mu;
-    // [dev][kind][grouped][pair-1][ksub-1][trace]
-    static size_t set[kMaxDeviceSlots][2][2][2][2][2] = {};
+    // [dev][kind][grouped][pair-1][ksub-1][mode]
+    static size_t set[kMaxDeviceSlots][2][2][2][2][3] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDeviceSlots) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(mu);
     for (int ksub = 1; ksub <= 2; ++ksub)
-        for (int tr = 0; tr < 2; ++tr) {
-            e = raise_smem_limit(select_kernel(kind, grouped, pair, ksub, tr != 0), smem,
-                                 &set[dev][kind][grouped ? 1 : 0][pair - 1][ksub - 1][tr]);
+        for (int mode = 0; mode < 3; ++mode) {
+            e = raise_smem_limit(select_kernel(kind, grouped, pair, ksub, mode), smem,
+                                 &set[dev][kind][grouped ? 1 : 0][pair - 1][ksub - 1][mode]);
             if (e != cudaSuccess) return e;
         }
     return cudaSuccess;
@@ -690,9 +799,9 @@ cudaError_t umma_check_registers(int kind, bool grouped, int pair, int* regs) {
     cudaFuncAttributes fa;
     const long need = 128L * kRegsWG0 + 128L * kRegsWG1;
     for (int ksub = 1; ksub <= 2; ++ksub)
-        for (int tr = 0; tr < 2; ++tr) {
+        for (int mode = 0; mode < 3; ++mode) {
             cudaError_t e =
-                cudaFuncGetAttributes(&fa, select_kernel(kind, grouped, pair, ksub, tr != 0));
+                cudaFuncGetAttributes(&fa, select_kernel(kind, grouped, pair, ksub, mode));
             if (e != cudaSuccess) return e;
             *regs = fa.numRegs;
             if (long(fa.numRegs) * kThreads < need) return cudaErrorInvalidConfiguration;
