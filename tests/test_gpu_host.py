@@ -89,3 +89,52 @@ def test_host_errors(gbr):
     with pytest.raises(ValueError):
         gbr.gemm_bias_relu_host(h.cuda().view(64, 64), h.view(64, 64), torch.zeros(64), dtype="ffma")
     gbr.check_device()
+
+
+def test_host_calls_from_two_threads(gbr):
+    """Two host threads, each on its own stream, calling at once: the library's
+    streams are shared, and each call's enqueue sequence is taken as a whole."""
+    import threading
+    jobs = []
+    for t in range(2):
+        A, B, bias = _host_inputs(1800, 520, 300, "bf16", seed=60 + t)
+        jobs.append((A, B, bias, torch.empty((1800, 520), dtype=torch.bfloat16).pin_memory(),
+                     torch.cuda.Stream()))
+    errors = []
+
+    def run(job):
+        try:
+            A, B, bias, C, st = job
+            for _ in range(3):
+                gbr.gemm_bias_relu_host(A, B, bias, C, dtype="bf16", stages=3, stream=st)
+        except Exception as e:   # surfaced below
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(j,)) for j in jobs]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    gbr.check_device()
+    for A, B, bias, C, _ in jobs:
+        ref = oracle.gemm_bias_relu(A.float(), B.float(), bias)
+        assert rel_frobenius(to_host_f64(C), ref) <= TOL["bf16"]
+
+
+def test_host_steps_on_two_streams_pipeline(gbr):
+    """Consecutive calls on two streams (as the benchmark issues them) each
+    produce their own correct result."""
+    A, B, bias = _host_inputs(2048, 512, 512, "bf16", seed=70)
+    outs = [torch.empty((2048, 512), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    with split_tail(gbr, 0):   # deterministic, so that the four results are comparable bit for bit
+        for i, C in enumerate(outs):
+            gbr.gemm_bias_relu_host(A, B, bias, C, dtype="bf16", stages=3, stream=streams[i % 2],
+                                    sync=False)
+        torch.cuda.synchronize()
+    gbr.check_device()
+    ref = oracle.gemm_bias_relu(A.float(), B.float(), bias)
+    for C in outs:
+        assert rel_frobenius(to_host_f64(C), ref) <= TOL["bf16"]
+        assert torch.equal(C, outs[0])
