@@ -97,7 +97,7 @@ def test_host_calls_from_two_threads(gbr):
     import threading
     jobs = []
     for t in range(2):
-        A, B, bias = _host_inputs(1800, 520, 300, "bf16", seed=60 + t)
+        A, B, bias = _host_inputs(1800, 520, 304, "bf16", seed=60 + t)
         jobs.append((A, B, bias, torch.empty((1800, 520), dtype=torch.bfloat16).pin_memory(),
                      torch.cuda.Stream()))
     errors = []
