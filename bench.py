@@ -313,7 +313,7 @@ def measure_workloads(gbr, peaks, sm_mhz=None, steps=20, warmup=3):
                   gemm_flops(256, 256, 256))
     out["gemm_fp32_256_ffma_S2"] = {"value": round(v, 3), "unit": "TFLOP/s",
                                     "us_per_call": round(ms * 1e3, 2),
-                                    "note": "4 CTAs of 128x128: launch/latency-bound"}
+                                    "note": "four 128x128 tiles on 4 of 152 SMs: bound by those SMs (the same replayed from a CUDA graph)"}
     counts, X, W, b = inputs.workload("grouped_bf16")
     dX, dW, db = X.cuda(), W.cuda(), b.cuda()
     dC = torch.empty((sum(counts), W.shape[2]), dtype=torch.bfloat16, device="cuda")
