@@ -232,6 +232,16 @@ def measure_copy(gbr, peaks, stages=4, steps=40, warmup=5):
         gbr.check_device()
         gbs = 2.0 * src.numel() * 4 * steps / t / 1e9
         out[S] = gbs
+    # The same S = 4 launches without programmatic dependent launch: each
+    # kernel starts only once the previous one has finished.
+    gbr.launch_overlap(False)
+    try:
+        t_plain = time_launches(lambda: gbr.staged_copy(src, dst, tile=(128, 64), stages=stages),
+                                steps, stream)
+    finally:
+        gbr.launch_overlap(True)
+    gbr.check_device()
+    plain_gbs = 2.0 * src.numel() * 4 * steps / t_plain / 1e9
     t_ref = time_launches(lambda: dst.copy_(src), steps, stream)
     torch_copy_gbs = 2.0 * src.numel() * 4 * steps / t_ref / 1e9
     best_S = max(out, key=out.get)
@@ -241,6 +251,7 @@ def measure_copy(gbr, peaks, stages=4, steps=40, warmup=5):
         "stages": stages, "value": round(achieved, 1), "unit": "GB/s",
         "by_stages": {str(k): round(v, 1) for k, v in out.items()}, "best_stages": best_S,
         "torch_copy_same_tensor_gbs": round(torch_copy_gbs, 1),
+        "without_launch_overlap_gbs": round(plain_gbs, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),

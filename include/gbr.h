@@ -237,6 +237,19 @@ int gbr_gemm_split_tail(int mode);
 int gbr_gemm_dynamic_schedule(int on);
 
 /*
+ * Programmatic dependent launch of the library's pipeline kernels (the
+ * staged copy, the FFMA and tensor-core GEMMs and the TF32 B transpose), for
+ * all later calls in the process.  on = 1 (default): each is launched so that
+ * it may be scheduled before the previous kernel in the stream has finished;
+ * its CTAs set up their barriers and Tensor Memory, then wait
+ * (griddepcontrol.wait) until that kernel has completed and its memory is
+ * visible, before any access to global memory.  Results and stream order are
+ * unchanged; back-to-back launches lose the gap between kernels.  on = 0:
+ * ordinary launches.  GBR_ERR_INVALID for other values.
+ */
+int gbr_launch_overlap(int on);
+
+/*
  * gemm_bias_relu_host -- gemm_bias_relu on HOST buffers: copies A, B and bias
  * to the device, computes, and copies C back, overlapping the three.  The
  * device buffers come from the library's stream-ordered pool.  M is cut into

@@ -9,7 +9,7 @@ Operators (C ABI in ``include/gbr.h``; this package is a thin ctypes binding):
 """
 from ._binding import (BF16, F32_FFMA, F32_TF32, OP_COPY, OP_GEMM, GbrError, check, check_device,
                        copy_tuning, device_status, gemm_dynamic_schedule, gemm_split_tail, gemm_tuning, gemm_bias_relu, gemm_bias_relu_grouped,
-                       gemm_bias_relu_host,
+                       gemm_bias_relu_host, launch_overlap,
                        last_error, launch_count, lib, library_path, max_stages,
                        selftest_copy_skip_load, selftest_gemm_skip_load, selftest_wait_timeout,
                        set_wait_timeout_ns, sm_count, staged_copy)
@@ -18,7 +18,7 @@ from ._build import build
 __all__ = [
     "BF16", "F32_FFMA", "F32_TF32", "OP_COPY", "OP_GEMM", "GbrError", "build", "check",
     "check_device", "copy_tuning", "device_status", "gemm_dynamic_schedule", "gemm_split_tail", "gemm_tuning", "gemm_bias_relu", "gemm_bias_relu_grouped", "gemm_bias_relu_host",
-    "last_error", "launch_count", "lib", "library_path", "max_stages", "selftest_copy_skip_load",
+    "last_error", "launch_count", "launch_overlap", "lib", "library_path", "max_stages", "selftest_copy_skip_load",
     "selftest_gemm_skip_load", "selftest_wait_timeout",
     "set_wait_timeout_ns", "sm_count", "staged_copy",
 ]

@@ -39,6 +39,7 @@ SIGNATURES = {
     "gbr_gemm_tuning": (_i32, [_i32, _i32, _i32, _i32]),
     "gbr_gemm_split_tail": (_i32, [_i32]),
     "gbr_gemm_dynamic_schedule": (_i32, [_i32]),
+    "gbr_launch_overlap": (_i32, [_i32]),
     "gbr_trace_buffer": (_i32, [_vp, _u64]),
     "gbr_selftest_wait_timeout": (_i32, [_u64, _vp]),
     "gbr_selftest_gemm_skip_load": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32,
@@ -256,6 +257,12 @@ def gemm_split_tail(mode: int = -1) -> None:
 def gemm_dynamic_schedule(on: bool) -> None:
     """Tensor-core GEMM tiles from an atomic counter (True) or the static order (see gbr.h)."""
     check(lib().gbr_gemm_dynamic_schedule(int(bool(on))))
+
+
+def launch_overlap(on: bool) -> None:
+    """Programmatic dependent launch of the library's kernels (True, default)
+    or ordinary launches (False) (see gbr.h)."""
+    check(lib().gbr_launch_overlap(int(bool(on))))
 
 
 def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:

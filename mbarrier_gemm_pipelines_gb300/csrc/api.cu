@@ -37,6 +37,7 @@ int g_gemm_l2_hint = -1;   // -1 auto (none): L2 policy of the operand loads
 int g_gemm_k_sub = -1;     // -1 auto (1): 128-byte K slices per ring stage
 int g_gemm_split = -1;     // -1 auto, 0 off, 1 on whenever some tile can be split
 int g_gemm_dynamic = 0;    // 1: tensor-core GEMMs take tiles from an atomic counter
+int g_launch_overlap = 1;  // 1: kernels are launched with programmatic stream serialization
 uint8_t* g_trace = nullptr;  // event trace buffer (device memory of the caller), or null
 uint32_t g_trace_cap = 0;    // records per (CTA, role)
 
@@ -391,6 +392,16 @@ int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
 void count_launch() { ++g_launches; }
 uint64_t wait_timeout_ns() { return timeout_ns(); }
 
+int programmatic_launch_attr(cudaLaunchAttribute* attr) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_launch_overlap) return 0;
+    }
+    attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr->val.programmaticStreamSerializationAllowed = 1;
+    return 1;
+}
+
 }  // namespace gbr
 
 using namespace gbr;
@@ -445,6 +456,13 @@ int gbr_gemm_dynamic_schedule(int on) {
         return fail(GBR_ERR_INVALID, "gbr_gemm_dynamic_schedule: on must be 0 or 1");
     std::lock_guard<std::mutex> lk(g_mu);
     g_gemm_dynamic = on;
+    return GBR_OK;
+}
+
+int gbr_launch_overlap(int on) {
+    if (on != 0 && on != 1) return fail(GBR_ERR_INVALID, "gbr_launch_overlap: on must be 0 or 1");
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_launch_overlap = on;
     return GBR_OK;
 }
 

@@ -155,6 +155,11 @@ cudaError_t launch_transpose_f32(const float* B, float* Bt, int K, int N, cudaSt
 // bits (0: none or never set up) and copies words [0..3] out, then clears them.
 uint32_t noalloc_take_status(uint32_t* words4);
 
+// Programmatic dependent launch (on unless gbr_launch_overlap(0)): fills
+// attr[0] and returns 1, or returns 0 when it is off.  Every kernel launched
+// with it runs griddep_wait() before its first global-memory access.
+int programmatic_launch_attr(cudaLaunchAttribute* attr);
+
 // ------------------------------------------------------------ api.cu services
 int report_error(int code, const char* msg);   // sets gbr_last_error(), returns code
 void count_launch();                           // adds one to gbr_launch_count()

@@ -142,6 +142,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&mapB);
     }
     __syncthreads();
+    // The set-up above overlaps the end of the previous kernel in the stream;
+    // no role touches global memory before that kernel is done.
+    ptx::griddep_wait();
 
     const uint32_t ring_base = ptx::smem_addr(ring);
 
@@ -192,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (pt == 0) trace_count(p.ctl, kRoleProducer, ntr);
+            ptx::griddep_launch_dependents();
             ptx::cp_async_wait_all();   // no copy may still be writing when the CTA exits
         } else if (warp == 0 && lane == 0) {
             // ------------------------------------------------ producer
@@ -221,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             trace_count(p.ctl, kRoleProducer, ntr);
+            ptx::griddep_launch_dependents();   // every load issued: the next launch may be scheduled
             if (*abort_flag) {
                 const uint32_t n = i < uint32_t(S) ? i : uint32_t(S);
                 for (uint32_t j = i - n; j < i; ++j)
@@ -378,11 +383,16 @@ cudaError_t ffma_check_registers(int* regs) {
 
 cudaError_t launch_gemm_ffma(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmShape& s,
                              int grid, size_t smem, cudaStream_t stream, bool cpasync) {
-    if (cpasync)
-        gemm_ffma_kernel<true><<<grid, kThreads, smem, stream>>>(mapA, mapB, s);
-    else
-        gemm_ffma_kernel<false><<<grid, kThreads, smem, stream>>>(mapA, mapB, s);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = programmatic_launch_attr(attr);
+    cfg.attrs = attr;
+    if (cpasync) return cudaLaunchKernelEx(&cfg, gemm_ffma_kernel<true>, mapA, mapB, s);
+    return cudaLaunchKernelEx(&cfg, gemm_ffma_kernel<false>, mapA, mapB, s);
 }
 
 }  // namespace gbr

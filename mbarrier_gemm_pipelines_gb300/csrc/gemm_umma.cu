@@ -385,6 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
+    // The set-up above overlaps the end of the previous kernel in the stream;
+    // no role touches global memory before that kernel is done.
+    ptx::griddep_wait();
 
     if (warp < 4) {
         ptx::setmaxnreg_dec<kRegsWG0>();
@@ -449,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (kTrace) trace_count(s.ctl, kRoleProducer, ntr);
+            ptx::griddep_launch_dependents();   // every load issued: the next launch may be scheduled
             if (*abort_flag && rank == 0) {
                 const uint32_t n = it < uint32_t(S) ? it : uint32_t(S);
                 for (uint32_t j = it - n; j < it; ++j)
@@ -746,13 +750,18 @@ cudaError_t launch_umma(int kind, int pair, const UmmaParams<GROUPED>& P, int gr
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = pair;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (pair == 2) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = pair;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    n += unsigned(programmatic_launch_attr(attr + n));
     cfg.attrs = attr;
-    cfg.numAttrs = pair == 2 ? 1 : 0;
+    cfg.numAttrs = n;
     void* args[] = {const_cast<UmmaParams<GROUPED>*>(&P)};
     const int mode = P.s.ctl.trace != nullptr ? 1 : P.s.dyn_counter != nullptr ? 2 : 0;
     return cudaLaunchKernelExC(&cfg, select_kernel(kind, GROUPED, pair, ksub_of(P.s), mode), args);

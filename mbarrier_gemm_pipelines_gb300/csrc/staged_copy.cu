@@ -42,6 +42,9 @@ __global__ void __launch_bounds__(64, 1)
         ptx::prefetch_tensormap(&dst_map);
     }
     __syncthreads();
+    // Everything above overlaps the end of the previous kernel in the stream;
+    // nothing below touches global memory before that kernel is done.
+    ptx::griddep_wait();
 
     const uint32_t ring_base = ptx::smem_addr(ring);
     // Every byte is read once and written once: optionally tell L2 to evict
@@ -69,6 +72,7 @@ __global__ void __launch_bounds__(64, 1)
                                  tr * a.tile_rows);
         }
         trace_count(a.ctl, kRoleProducer, nt);
+        ptx::griddep_launch_dependents();   // every load issued: the next launch may be scheduled
         if (*abort_flag) {
             // Let this CTA's own loads in flight land before the CTA exits.
             const uint32_t n = i < uint32_t(S) ? i : uint32_t(S);
@@ -134,8 +138,15 @@ cudaError_t copy_occupancy(size_t smem, int* blocks_per_sm) {
 
 cudaError_t launch_staged_copy(const CUtensorMap& src, const CUtensorMap& dst, const CopyArgs& a,
                                int grid, size_t smem, cudaStream_t stream) {
-    staged_copy_kernel<<<grid, 64, smem, stream>>>(src, dst, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(64);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = programmatic_launch_attr(attr);
+    cfg.attrs = attr;
+    return cudaLaunchKernelEx(&cfg, staged_copy_kernel, src, dst, a);
 }
 
 }  // namespace gbr

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(kThreadsX * kThreadsY)
     __shared__ float tile[kT][kT + 1];
     const int n0 = blockIdx.x * kT, k0 = blockIdx.y * kT;
     const int tx = threadIdx.x, ty = threadIdx.y;
+    ptx::griddep_wait();                 // B may come from the previous kernel in the stream
+    ptx::griddep_launch_dependents();    // the GEMM that reads Bt may be scheduled (it waits too)
     // Load rows k0..k0+63, columns n0 + 4tx .. +3 (N is a multiple of 4).
 #pragma unroll
     for (int r = ty; r < kT; r += kThreadsY) {
@@ -52,8 +54,14 @@ __global__ void __launch_bounds__(kThreadsX * kThreadsY)
 cudaError_t launch_transpose_f32(const float* B, float* Bt, int K, int N, cudaStream_t stream) {
     dim3 grid((N + kT - 1) / kT, (K + kT - 1) / kT);
     dim3 block(kThreadsX, kThreadsY);
-    transpose_f32_kernel<<<grid, block, 0, stream>>>(B, Bt, K, N);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = programmatic_launch_attr(attr);
+    cfg.attrs = attr;
+    return cudaLaunchKernelEx(&cfg, transpose_f32_kernel, B, Bt, K, N);
 }
 
 }  // namespace gbr
