@@ -216,6 +216,27 @@ def time_launches(fn, steps, stream):
     return start.elapsed_time(end) / 1e3
 
 
+def time_each(fn, steps, stream):
+    """Each launch between its own pair of events (a separate pass, outside the
+    timed region): the per-step distribution, in seconds."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for i in range(steps):
+        fn()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [evs[i].elapsed_time(evs[i + 1]) / 1e3 for i in range(steps)]
+
+
+def step_stats(times, work, scale):
+    """Median and minimum of per-step times, with the throughput each gives."""
+    med, lo = statistics.median(times), min(times)
+    return {"steps": len(times), "median_ms": round(med * 1e3, 4), "min_ms": round(lo * 1e3, 4),
+            "value_at_median": round(work / med / scale, 2), "value_at_min": round(work / lo / scale, 2)}
+
+
 def measure_copy(gbr, peaks, stages=4, steps=40, warmup=5):
     import torch
     from mbarrier_gemm_pipelines_gb300 import inputs
@@ -242,6 +263,9 @@ def measure_copy(gbr, peaks, stages=4, steps=40, warmup=5):
         gbr.launch_overlap(True)
     gbr.check_device()
     plain_gbs = 2.0 * src.numel() * 4 * steps / t_plain / 1e9
+    per_step = step_stats(time_each(lambda: gbr.staged_copy(src, dst, tile=(128, 64), stages=stages),
+                                    20, stream), 2.0 * src.numel() * 4, 1e9)
+    gbr.check_device()
     t_ref = time_launches(lambda: dst.copy_(src), steps, stream)
     torch_copy_gbs = 2.0 * src.numel() * 4 * steps / t_ref / 1e9
     best_S = max(out, key=out.get)
@@ -252,6 +276,7 @@ def measure_copy(gbr, peaks, stages=4, steps=40, warmup=5):
         "by_stages": {str(k): round(v, 1) for k, v in out.items()}, "best_stages": best_S,
         "torch_copy_same_tensor_gbs": round(torch_copy_gbs, 1),
         "without_launch_overlap_gbs": round(plain_gbs, 1),
+        "per_step": per_step,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -418,6 +443,8 @@ def run_ours(args):
     clocks = sampler.stop()
     gbr.check_device()
     flops = gemm_flops(M, N, K)
+    per_step = step_stats(time_each(step, 20, stream), flops, 1e12)
+    gbr.check_device()
     value, t = aggregate(t, flops * args.steps, world)
     value /= 1e12
     per_launch = t / args.steps
@@ -498,6 +525,8 @@ def run_ours(args):
                 "steps": e2e_steps, "api": "gemm_bias_relu_host (C ABI, pinned host buffers)",
                 "streams": 2},
         "gpu_launches": int(launches),
+        "per_step": dict(per_step, note="a separate pass after the timed region, each launch "
+                                        "between its own events"),
         "clocks": clocks,
         "cpu_baseline": cpu,
         "staged_copy": copy,
