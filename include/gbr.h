@@ -10,6 +10,7 @@
  *
  *   gemm_bias_relu          C = ReLU(A * B + bias)
  *   gemm_bias_relu_grouped  the same per expert segment (MoE-style), one launch
+ *   gemm_bias_relu_host     gemm_bias_relu on host buffers, copies overlapped
  *   staged_copy             gmem -> smem -> gmem through the ring (TMA both ways)
  *
  * Conventions shared by every entry point
@@ -27,7 +28,9 @@
  *     multiple of 16 bytes (the TMA rule): fp32 row lengths a multiple of 4,
  *     bf16 row lengths a multiple of 8.  Otherwise GBR_ERR_ALIGN.
  *   - The library keeps, per device, a 64-byte status block it allocates on
- *     first use, plus cached device attributes.
+ *     first use, a memory pool for per-call scratch (taken and returned in
+ *     stream order: the TF32 Bt copy, split-tile sums, the tile counter), the
+ *     streams and events of gemm_bias_relu_host, and cached device attributes.
  */
 #ifndef GBR_H_
 #define GBR_H_
