@@ -544,7 +544,9 @@ def run_reference(args):
     from mbarrier_gemm_pipelines_gb300 import inputs
     oracle.build()
     A, B, bias = inputs.workload("gemm_bf16")
-    per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    A, B, bias = A.float(), B.float(), bias.float()   # widened once, not per step
+    # About 150 s of oracle work over the whole run, at least 0.25 s per step.
+    per_step = max(0.25, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         cpu_gemm_sample(A, B, bias, target_s=per_step)
     vals, rows_used, secs = [], 0, 0.0
