@@ -91,3 +91,40 @@ def test_switch_is_validated(gbr):
     with pytest.raises(gbr.GbrError):
         gbr.check(gbr.lib().gbr_launch_overlap(2))
     gbr.launch_overlap(True)
+
+
+def _random_sequence(gbr, seed, n_ops=60):
+    """A seeded random program over four 512 x 512 fp32 buffers: staged copies,
+    FFMA and TF32 GEMMs and torch kernels, each reading buffers earlier ops
+    wrote; returns the buffers at the end."""
+    g = torch.Generator().manual_seed(seed)
+    bufs = [torch.rand(512, 512, generator=g).cuda() for _ in range(4)]
+    bias = (torch.rand(512, generator=g) - 0.5).cuda()
+    for _ in range(n_ops):
+        op = int(torch.randint(0, 4, (1,), generator=g))
+        i, j, k = (int(x) for x in torch.randperm(4, generator=g)[:3])
+        if op == 0:
+            gbr.staged_copy(bufs[i], bufs[k], tile=(128, 64), stages=int(torch.randint(1, 8, (1,), generator=g)))
+        elif op in (1, 2):
+            gbr.gemm_bias_relu(bufs[i], bufs[j], bias, bufs[k], dtype="ffma" if op == 1 else "tf32",
+                               stages=3)
+            bufs[k].div_(bufs[k].amax().clamp_min(1e-3))     # torch kernels: keep values in [0, 1]
+        else:
+            bufs[k].mul_(0.75).add_(bufs[i], alpha=0.25)
+    torch.cuda.synchronize()
+    gbr.check_device()
+    return [b.clone() for b in bufs]
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_random_dependent_sequence_equals_plain(gbr, seed):
+    with split_tail(gbr, 0):
+        gbr.launch_overlap(True)
+        got = _random_sequence(gbr, seed)
+        gbr.launch_overlap(False)
+        try:
+            ref = _random_sequence(gbr, seed)
+        finally:
+            gbr.launch_overlap(True)
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
