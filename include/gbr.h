@@ -23,7 +23,8 @@
  *     failures, with a message available from gbr_last_error() on the calling
  *     thread.  Nothing is launched when validation fails.
  *   - Device-side failures (a pipeline wait that exceeded its time limit) are
- *     reported by gbr_device_status(), which also clears them.
+ *     reported by gbr_device_status(), which also clears them.  The status
+ *     block keeps the FIRST timeout recorded since the last read.
  *   - Global addresses must be 16-byte aligned and every row pitch must be a
  *     multiple of 16 bytes (the TMA rule): fp32 row lengths a multiple of 4,
  *     bf16 row lengths a multiple of 8.  Otherwise GBR_ERR_ALIGN.
@@ -145,11 +146,13 @@ int staged_copy(const void *src, void *dst, int64_t rows, int64_t cols, int tile
 
 /*
  * gbr_device_status -- synchronises `stream`, then reports and clears the
- * current device's status block.  GBR_OK, GBR_ERR_TIMEOUT (a pipeline wait in
- * a kernel exceeded its limit; the kernel raised its abort flag, let its own
- * copies in flight finish, released its Tensor Memory and returned, so the
- * context stays usable; the output of that call is undefined), or
- * GBR_ERR_CUDA for a CUDA error seen while synchronising.
+ * current device's status block (and the status words of
+ * gemm_bias_relu_tf32_noalloc).  It allocates nothing.  Returns GBR_OK,
+ * GBR_ERR_TIMEOUT (a pipeline wait in a kernel exceeded its limit; the kernel
+ * raised its abort flag, let its own copies in flight finish, released its
+ * Tensor Memory and returned, so the context stays usable; the output of
+ * that call is undefined), or GBR_ERR_CUDA for a CUDA error seen while
+ * synchronising.
  */
 int gbr_device_status(gbr_stream_t stream);
 
@@ -218,7 +221,11 @@ int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage);
  * only by the order of fp32 additions; that order follows the arrival of the
  * parts, so a split tile can differ in its last bits from run to run (mode 0
  * makes every launch deterministic).
- *   mode -1: auto (split when the last round shrinks by >= 1/8 of a tile),
+ *   mode -1: auto (the default): split when the last round shrinks by >= 1/8
+ *         of a tile and the predicted saving is >= 1/20 (5%) of the launch's
+ *         time; below that the measured gain is within run-to-run noise, so
+ *         such launches stay deterministic bit for bit (bf16 8192^3 on a
+ *         152-SM GB300 does not split; TF32 4096^3 does).
  *         0: never, 1: whenever some tile can be split.
  * GBR_ERR_INVALID for other values.  The failure-detection self tests and
  * gemm_bias_relu_tf32_noalloc never split.
@@ -315,8 +322,12 @@ int gbr_selftest_wait_timeout(uint64_t timeout_ns, gbr_stream_t stream);
  * exist in that launch nothing is planted and the call completes normally.
  *
  * gbr_selftest_gemm_skip_load: arguments as gemm_bias_relu; dtype GBR_F32_FFMA,
- *   GBR_F32_TF32 or GBR_BF16 (the tensor-core dtypes run one CTA per tile, so
- *   `stages` must fit that kernel).
+ *   GBR_F32_TF32 or GBR_BF16.  The tensor-core dtypes run one CTA per tile
+ *   (`stages` must fit that kernel), unless gbr_gemm_tuning forces the CTA
+ *   pair (cta_pair = 2): then `cta` names the pair (unit), both of whose CTAs
+ *   leave item `item` unfilled, and the CTA reported is either CTA of it.
+ *   After an abort the even CTA of a pair also waits for the loads its peer
+ *   issued before either CTA exits.
  * gbr_selftest_copy_skip_load: arguments as staged_copy with 128 x 64 tiles.
  * Returns GBR_OK when launched, GBR_ERR_INVALID for a negative cta or item or
  * a limit out of range, and the errors of the wrapped call.
@@ -336,26 +347,48 @@ int gbr_selftest_copy_skip_load(const void *src, void *dst, int64_t rows, int64_
  * or synchronise the device at unpredictable times), plug-ins whose host
  * framework owns all device allocation, and processes whose device memory is
  * entirely reserved by another allocator, so that an allocation from this
- * library would fail.  The TF32 path needs K*N*4 bytes of scratch for a K-major copy of
- * B plus status words; here both live in one file-scope device array of
- * 16 MiB + 256 bytes that the CUDA driver creates for every device that loads
- * this library and keeps until the process exits.  This call allocates nothing.
+ * library would fail.  This variant takes a K-major copy of B (K*N*4 bytes,
+ * made by a transpose kernel) and its status words from one file-scope
+ * device array of 16 MiB + 256 bytes, which the CUDA driver creates on every
+ * device that loads this library and keeps until the process exits.  The call
+ * allocates nothing, and neither does gbr_device_status().
  *
  *   A [M, K], B [K, N], bias [N], C [M, N]: fp32, as for gemm_bias_relu;
- *   caller-owned device memory.  K and N multiples of 4.
+ *   caller-owned device memory.  K and N multiples of 4.  C must not overlap
+ *   A, B or bias (GBR_ERR_INVALID).
  *   K * N must be <= 4194304 (K*N*4 bytes <= 16 MiB): larger sizes return
  *   GBR_ERR_INVALID without launching anything.
- *   stages, stream: as for gemm_bias_relu.
+ *   stages: 1..4 -- this call always runs one CTA per 128x256 tile, whose
+ *   ring holds 4 stages on GB300; gbr_max_stages() reports the CTA-pair
+ *   kernel's larger limit, which does not apply here (GBR_ERR_SMEM).
+ *   stream: as for gemm_bias_relu.
  * The first call on a device looks up the array's device address (once, with
- * that device current); make that first call before any stream capture.
- * Every call uses the same array: calls that may overlap on the GPU (different
- * streams, or several devices' work racing on one array) race and give
- * undefined results -- serialise them.  Each call clears the status words
- * before use; gbr_device_status() reports a wait timeout recorded there.
+ * that device current) and clears its status words, synchronising the
+ * device; make that first call before any stream capture.
+ * The array exists once per device, and every call on that device uses it:
+ * calls on one device that may overlap on the GPU (different streams, or
+ * several host threads) race and give undefined results -- serialise them.
+ * Calls on different devices use different arrays.
+ * Status: a wait that times out records its site in the array's status
+ * words, which keep the FIRST timeout recorded until gbr_device_status(),
+ * called with the stream the calls ran on, reads and clears them; timeouts
+ * of later calls before that read are not reported separately.
  */
 int gemm_bias_relu_tf32_noalloc(const float *A, const float *B, const float *bias, float *C,
                                 int64_t M, int64_t N, int64_t K, int stages,
                                 gbr_stream_t stream);
+
+/*
+ * Failure-detection self test of gemm_bias_relu_tf32_noalloc: the same call
+ * with one ring stage left unfilled (CTA `cta`, ring item `item`, limit
+ * `limit_ns`), exactly as gbr_selftest_gemm_skip_load does for
+ * gemm_bias_relu.  The timeout lands in the no-alloc array's status words,
+ * and gbr_device_status() reports it (GBR_ERR_TIMEOUT, site 0x31 MMA issuer
+ * or 0x41 epilogue, or the producer's 0x11).  Allocates nothing.
+ */
+int gbr_selftest_noalloc_skip_load(const float *A, const float *B, const float *bias, float *C,
+                                   int64_t M, int64_t N, int64_t K, int stages, int cta, int item,
+                                   uint64_t limit_ns, gbr_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -8,10 +8,12 @@ Operators (C ABI in ``include/gbr.h``; this package is a thin ctypes binding):
 * ``staged_copy``             TMA gmem -> smem -> gmem through an S-slot ring.
 """
 from ._binding import (BF16, F32_FFMA, F32_TF32, OP_COPY, OP_GEMM, GbrError, check, check_device,
-                       copy_tuning, device_status, gemm_dynamic_schedule, gemm_split_tail, gemm_tuning, gemm_bias_relu, gemm_bias_relu_grouped,
+                       copy_tuning, device_status, gemm_dynamic_schedule, gemm_split_tail,
+                       gemm_tuning, gemm_bias_relu, gemm_bias_relu_grouped,
                        gemm_bias_relu_host, launch_overlap,
                        last_error, launch_count, lib, library_path, max_stages,
-                       selftest_copy_skip_load, selftest_gemm_skip_load, selftest_wait_timeout,
+                       gemm_bias_relu_tf32_noalloc, selftest_copy_skip_load, selftest_gemm_skip_load,
+                       selftest_noalloc_skip_load, selftest_wait_timeout,
                        set_wait_timeout_ns, sm_count, staged_copy)
 from ._build import build
 
@@ -19,6 +21,7 @@ __all__ = [
     "BF16", "F32_FFMA", "F32_TF32", "OP_COPY", "OP_GEMM", "GbrError", "build", "check",
     "check_device", "copy_tuning", "device_status", "gemm_dynamic_schedule", "gemm_split_tail", "gemm_tuning", "gemm_bias_relu", "gemm_bias_relu_grouped", "gemm_bias_relu_host",
     "last_error", "launch_count", "launch_overlap", "lib", "library_path", "max_stages", "selftest_copy_skip_load",
-    "selftest_gemm_skip_load", "selftest_wait_timeout",
+    "selftest_gemm_skip_load", "selftest_wait_timeout", "gemm_bias_relu_tf32_noalloc",
+    "selftest_noalloc_skip_load",
     "set_wait_timeout_ns", "sm_count", "staged_copy",
 ]

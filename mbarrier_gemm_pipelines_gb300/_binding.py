@@ -46,6 +46,8 @@ SIGNATURES = {
                                            _i32, _u64, _vp]),
     "gbr_selftest_copy_skip_load": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _i32, _u64, _vp]),
     "gemm_bias_relu_tf32_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
+    "gbr_selftest_noalloc_skip_load": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32,
+                                              _i32, _u64, _vp]),
 }
 
 _lib = None
@@ -300,20 +302,45 @@ def selftest_copy_skip_load(src, stages, cta, item, limit_ns, stream=None):
     return dst
 
 
+def _noalloc_shapes(A, B, bias, C):
+    """The dimension checks of gemm_bias_relu, for the no-alloc entry points
+    (which take C from the caller): nothing is launched when they fail."""
+    import torch
+    for t, n in ((A, "A"), (B, "B"), (bias, "bias"), (C, "C")):
+        _cuda_tensor(t, n, (torch.float32,))
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(bias.shape) != (N,):
+        raise ValueError("shape mismatch: A %s, B %s, bias %s" % (tuple(A.shape), tuple(B.shape),
+                                                                  tuple(bias.shape)))
+    if tuple(C.shape) != (M, N):
+        raise ValueError("C must be [M, N] = [%d, %d], got %s" % (M, N, tuple(C.shape)))
+    return M, N, K
+
+
 def gemm_bias_relu_tf32_noalloc(A, B, bias, C, stages=4, stream=None):
     """TF32 C = ReLU(A @ B + bias) that allocates no device memory (C is required).
 
     For callers that may not allocate: serving loops that must stay out of
     allocators, plug-ins whose host framework owns all device allocation,
-    processes whose device memory is reserved by another allocator.  Scratch comes from a fixed 16 MiB device
-    array shared by all calls (K * N <= 4194304); calls that overlap on the GPU
-    race, so serialise them."""
-    import torch
-    for t, n in ((A, "A"), (B, "B"), (bias, "bias"), (C, "C")):
-        _cuda_tensor(t, n, (torch.float32,))
-    M, K = A.shape
-    N = B.shape[1]
+    processes whose device memory is reserved by another allocator.  Scratch
+    comes from a fixed 16 MiB device array that every call on the device
+    shares (K * N <= 4194304); calls that overlap on the GPU race, so
+    serialise them.  One CTA per tile: stages 1..4."""
+    M, N, K = _noalloc_shapes(A, B, bias, C)
     check(lib().gemm_bias_relu_tf32_noalloc(A.data_ptr(), B.data_ptr(), bias.data_ptr(),
                                             C.data_ptr(), M, N, K, int(stages),
                                             _stream_ptr(stream)))
+    return C
+
+
+def selftest_noalloc_skip_load(A, B, bias, C, stages, cta, item, limit_ns, stream=None):
+    """Runs gemm_bias_relu_tf32_noalloc with one stage of CTA `cta`, ring item
+    `item`, left unfilled (see gbr.h); C's contents are then undefined."""
+    M, N, K = _noalloc_shapes(A, B, bias, C)
+    check(lib().gbr_selftest_noalloc_skip_load(A.data_ptr(), B.data_ptr(), bias.data_ptr(),
+                                               C.data_ptr(), M, N, K, int(stages), int(cta),
+                                               int(item), int(limit_ns), _stream_ptr(stream)))
     return C

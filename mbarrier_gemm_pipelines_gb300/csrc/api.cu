@@ -58,8 +58,8 @@ struct DevCtx {
     cudaEvent_t host_events[kHostEvents] = {};
     std::mutex host_mu;
     bool ffma_regs_ok = false, ffma_regs_checked = false;
-    bool umma_regs_ok[2][2][2] = {};        // [kind][grouped][pair - 1]
-    bool umma_regs_checked[2][2][2] = {};
+    bool umma_regs_ok[kUmmaKinds][2][2] = {};        // [kind][grouped][pair - 1]
+    bool umma_regs_checked[kUmmaKinds][2][2] = {};
 };
 DevCtx g_dev[kMaxDevices];
 
@@ -254,6 +254,11 @@ int umma_max_stages(int pair, int smem_optin, int k_sub = 1) {
     return max_stages_for(pair == 2 ? umma2_bytes_fn : umma1_bytes_fn, smem_optin);
 }
 
+int pair_forced() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_gemm_pair;
+}
+
 int k_sub_forced() {
     std::lock_guard<std::mutex> lk(g_mu);
     return g_gemm_k_sub;
@@ -390,7 +395,8 @@ int check_umma_regs(DevCtx& c, int kind, bool grouped, int pair) {
 
 int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
 void count_launch() { ++g_launches; }
-uint64_t wait_timeout_ns() { return timeout_ns(); }
+uint64_t wait_timeout_ns() { return t_timeout_override ? t_timeout_override : timeout_ns(); }
+FaultInjection injection_now() { return t_inject; }
 
 int programmatic_launch_attr(cudaLaunchAttribute* attr) {
     {
@@ -510,13 +516,23 @@ int gbr_max_stages(int op, int dtype, int tile_rows, int tile_cols) {
 }
 
 int gbr_device_status(gbr_stream_t stream) {
-    DevCtx* c;
-    int r = get_ctx(&c);
-    if (r != GBR_OK) return r;
-    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    // Allocates nothing: the regular status block is read only if a regular
+    // call has already set up this device (none can have recorded anything
+    // otherwise), so callers of gemm_bias_relu_tf32_noalloc may use this too.
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(GBR_ERR_INVALID, "device %d out of range", dev);
+    uint32_t* status = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_dev[dev].ready) status = g_dev[dev].status;
+    }
+    e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    uint32_t st[kStatusWords];
-    if ((e = cudaMemcpy(st, c->status, sizeof(st), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    uint32_t st[kStatusWords] = {};
+    if (status != nullptr &&
+        (e = cudaMemcpy(st, status, sizeof(st), cudaMemcpyDeviceToHost)) != cudaSuccess)
         return cuda_fail(e, "reading the status block");
     if (st[0] == 0) {
         // Calls of gemm_bias_relu_tf32_noalloc record into their own scratch array.
@@ -527,7 +543,7 @@ int gbr_device_status(gbr_stream_t stream) {
                     "%u, item %u); that call's output is undefined",
                     na[1], na[2], na[3]);
     }
-    if ((e = cudaMemset(c->status, 0, sizeof(st))) != cudaSuccess)
+    if ((e = cudaMemset(status, 0, sizeof(st))) != cudaSuccess)
         return cuda_fail(e, "clearing the status block");
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
     return fail(GBR_ERR_TIMEOUT,
@@ -543,6 +559,14 @@ int gbr_selftest_gemm_skip_load(const void* A, const void* B, const float* bias,
         return fail(GBR_ERR_UNSUPPORTED, "self test: runs on the TMA-fed rings only");
     return with_injection(cta, item, limit_ns, [&] {
         return gemm_bias_relu(A, B, bias, C, M, N, K, dtype, stages, stream);
+    });
+}
+
+int gbr_selftest_noalloc_skip_load(const float* A, const float* B, const float* bias, float* C,
+                                   int64_t M, int64_t N, int64_t K, int stages, int cta, int item,
+                                   uint64_t limit_ns, gbr_stream_t stream) {
+    return with_injection(cta, item, limit_ns, [&] {
+        return gemm_bias_relu_tf32_noalloc(A, B, bias, C, M, N, K, stages, stream);
     });
 }
 
@@ -757,14 +781,16 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
     const uint32_t panel_cols = uint32_t(128 / es);  // B panel width; also the C store box width
     int pair = 1;
     if ((r = choose_pair(M, stages, c->smem_optin, &pair)) != GBR_OK) return r;
-    if (s.inject.enabled) {
-        // The self test runs one CTA per tile: there the abort path drains
-        // exactly the loads its own producer issued.
+    if (s.inject.enabled && pair_forced() != 2) {
+        // The self test runs one CTA per tile unless gbr_gemm_tuning forces
+        // the CTA pair; `cta` then names the pair, both of whose CTAs leave
+        // the item unfilled.
         if (stages > umma_max_stages(1, c->smem_optin))
             return fail(GBR_ERR_SMEM, "self test: stages must fit one CTA per tile");
         pair = 1;
     }
-    s.k_sub = uint32_t(s.inject.enabled ? 1 : choose_k_sub(pair, stages, c->smem_optin));
+    s.k_sub = uint32_t(s.inject.enabled && pair == 1 ? 1
+                                                     : choose_k_sub(pair, stages, c->smem_optin));
     s.m_tiles = int32_t(cdiv(M, int64_t(kUmmaBM) * pair));
     s.n_tiles = int32_t(cdiv(N, kUmmaBN));
     s.num_kb = int32_t(cdiv(K, int64_t(bk) * s.k_sub));
@@ -789,6 +815,7 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
                            CU_TENSOR_MAP_SWIZZLE_128B, "A")) != GBR_OK)
             return r;
         if (kind == kUmmaBf16) {
+            // B row-major [K, N] as N-major panels of panel_cols x bk (MN-major operand).
             if ((r = encode_2d(&mb, dt, B, uint64_t(N), uint64_t(K), uint64_t(N) * es, panel_cols,
                                bk, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != GBR_OK)
                 return r;

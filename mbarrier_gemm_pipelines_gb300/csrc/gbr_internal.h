@@ -38,6 +38,13 @@ __device__ __forceinline__ bool inject_skip(const FaultInjection& f, uint32_t it
     return f.enabled != 0 && int32_t(blockIdx.x) == f.cta && int32_t(item) == f.item;
 }
 
+// The same for kernels whose CTAs work in units that share each ring item (a
+// CTA pair): `cta` names the unit, and every CTA of it skips that item's loads.
+__device__ __forceinline__ bool inject_skip_unit(const FaultInjection& f, uint32_t unit,
+                                                 uint32_t item) {
+    return f.enabled != 0 && int32_t(unit) == f.cta && int32_t(item) == f.item;
+}
+
 // ------------------------------------------------------------ staged copy
 struct CopyArgs {
     int32_t rows, cols;            // fp32 elements
@@ -117,7 +124,10 @@ constexpr uint32_t kUmmaStageBytes = kUmmaAStageBytes + kUmmaBStageBytes;
 constexpr uint32_t kUmmaEpiBytes = 4 * 2 * 32 * 128;        // 4 warps x 2 buffers x 4 KiB
 constexpr int kMaxGroups = 32;
 
+// bf16 (B read MN-major from B[K, N]); TF32 (B read K-major from a transposed
+// copy Bt[N, K] that a pre-pass kernel writes).
 enum UmmaKind : int { kUmmaBf16 = 0, kUmmaTf32 = 1 };
+constexpr int kUmmaKinds = 2;
 
 struct GroupTable {
     int32_t num_groups;
@@ -163,7 +173,8 @@ int programmatic_launch_attr(cudaLaunchAttribute* attr);
 // ------------------------------------------------------------ api.cu services
 int report_error(int code, const char* msg);   // sets gbr_last_error(), returns code
 void count_launch();                           // adds one to gbr_launch_count()
-uint64_t wait_timeout_ns();                    // current per-wait limit
+uint64_t wait_timeout_ns();                    // per-wait limit of this thread's next launch
+FaultInjection injection_now();                // self-test fault of this thread's next launch
 
 // ------------------------------------------------------------ self test
 cudaError_t launch_wait_selftest(KernelCtl ctl, cudaStream_t stream);

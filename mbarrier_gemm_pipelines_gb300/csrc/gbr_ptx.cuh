@@ -56,6 +56,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Counts `bytes` of the current phase's expected transactions as done without
+// any data (used only while tearing down, for bytes that were registered but
+// whose copy was never issued).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
 // Upper bound, in ns, on how long one try_wait may keep the thread suspended
 // before it returns false.  The hardware wakes the thread as soon as the phase
 // completes; without a hint the instruction returns after a short
@@ -319,6 +327,13 @@ __device__ __forceinline__ void cluster_sync_all() {
 // 32-bit store to shared memory of a CTA of the cluster (mapa address).
 __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// 32-bit load from shared memory of a CTA of the cluster (mapa address).
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {

@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::griddep_wait();
 
     const uint32_t ring_base = ptx::smem_addr(ring);
+    uint32_t issued = 0;   // TMA producer lane: ring items registered on full[]
 
     if (warp < 4) {
         ptx::setmaxnreg_dec<kProducerRegs>();
@@ -226,11 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             trace_count(p.ctl, kRoleProducer, ntr);
             ptx::griddep_launch_dependents();   // every load issued: the next launch may be scheduled
-            if (*abort_flag) {
-                const uint32_t n = i < uint32_t(S) ? i : uint32_t(S);
-                for (uint32_t j = i - n; j < i; ++j)
-                    mbar_wait_drain(ptx::smem_addr(full + j % S), (j / S) & 1u, p.ctl.timeout_ns);
-            }
+            issued = i;
         }
     } else {
         ptx::setmaxnreg_inc<kConsumerRegs>();
@@ -277,6 +274,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tracer) trace_count(p.ctl, kRoleConsumer, ntr);
     }
     __syncwarp();
+    __syncthreads();
+    // Every role has left its loop, so the abort flag is final.  After an
+    // abort the TMA lane waits (bounded) for its loads still in flight -- the
+    // last S items it registered, except a self test's unissued one -- before
+    // the CTA may exit.  (The cp.async producers waited for their own copies.)
+    if (!CPASYNC && warp == 0 && lane == 0 && *abort_flag) {
+        const uint32_t n = issued < uint32_t(S) ? issued : uint32_t(S);
+        for (uint32_t j = issued - n; j < issued; ++j)
+            if (!inject_skip(p.inject, j))
+                mbar_wait_drain(ptx::smem_addr(full + j % S), (j / S) & 1u, p.ctl.timeout_ns);
+    }
     __syncthreads();
 }
 

@@ -19,6 +19,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -95,6 +96,11 @@ int na_setup(NoallocDevice** out) {
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr)
             return report_error(GBR_ERR_CUDA, "cudaGetSymbolAddress(no-alloc scratch) failed");
+        // The array starts zeroed when the module loads; clear its status words
+        // once more here, and wait, so that no launch can overtake the clear.
+        if (cudaMemset(p, 0, kNoallocStatusBytes) != cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess)
+            return report_error(GBR_ERR_CUDA, "clearing the no-alloc status words failed");
         int regs = 0;
         d.regs_ok = umma_check_registers(kUmmaTf32, false, &regs) == cudaSuccess;
         d.scratch = static_cast<unsigned char*>(p);
@@ -106,8 +112,12 @@ int na_setup(NoallocDevice** out) {
 
 }  // namespace
 
-// Reads and clears the status words of the no-alloc scratch on the current
-// device; 0 if nothing was recorded or the scratch was never set up there.
+// Reads the status words of the no-alloc scratch on the current device and,
+// when a timeout is recorded there, clears them and waits for the clear (so
+// that no later launch can overtake it).  The caller has synchronised the
+// stream the no-alloc calls ran on.  Returns the error bits (0: nothing
+// recorded, or the scratch was never set up on this device) and copies words
+// [0..3] out; allocates nothing.
 uint32_t noalloc_take_status(uint32_t* words4) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
@@ -121,6 +131,7 @@ uint32_t noalloc_take_status(uint32_t* words4) {
     if (cudaMemcpy(st, scratch, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return 0;
     if (st[0] == 0) return 0;
     cudaMemset(scratch, 0, sizeof(st));
+    cudaDeviceSynchronize();
     for (int i = 0; i < 4; ++i) words4[i] = st[i];
     return st[0];
 }
@@ -142,9 +153,19 @@ extern "C" int gemm_bias_relu_tf32_noalloc(const float* A, const float* B, const
     NoallocDevice* d;
     int r = na_setup(&d);
     if (r != GBR_OK) return r;
-    const size_t ring_bytes = 1024 + size_t(stages) * kUmmaStageBytes + kUmmaEpiBytes + 256;
-    if (stages < 1 || ring_bytes > size_t(d->smem_optin))
-        return report_error(GBR_ERR_SMEM, "gemm_bias_relu_tf32_noalloc: stages out of range");
+    // One CTA per 128x256 tile: as many 48 KiB stages as fit beside the
+    // epilogue staging (4 on GB300).
+    int smax = 0;
+    while (smax < 16 && 1024 + size_t(smax + 1) * kUmmaStageBytes + kUmmaEpiBytes + 256 <=
+                            size_t(d->smem_optin))
+        ++smax;
+    if (stages < 1 || stages > smax) {
+        char msg[160];
+        snprintf(msg, sizeof(msg),
+                 "gemm_bias_relu_tf32_noalloc: stages=%d outside [1, %d] (one CTA per tile)",
+                 stages, smax);
+        return report_error(GBR_ERR_SMEM, msg);
+    }
     if (M == 0 || N == 0) return GBR_OK;
     if (!C || !bias || (K > 0 && (!A || !B)))
         return report_error(GBR_ERR_INVALID, "gemm_bias_relu_tf32_noalloc: NULL buffer");
@@ -153,15 +174,25 @@ extern "C" int gemm_bias_relu_tf32_noalloc(const float* A, const float* B, const
         return report_error(GBR_ERR_ALIGN,
                             "gemm_bias_relu_tf32_noalloc: 16-byte aligned buffers, K and N "
                             "multiples of 4");
+    auto overlap = [](const void* a, size_t an, const void* b, size_t bn) {
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+        return a0 < b0 + bn && b0 < a0 + an;
+    };
+    const size_t c_bytes = size_t(M) * size_t(N) * 4u;
+    if ((K > 0 && (overlap(C, c_bytes, A, size_t(M) * size_t(K) * 4u) ||
+                   overlap(C, c_bytes, B, size_t(K) * size_t(N) * 4u))) ||
+        overlap(C, c_bytes, bias, size_t(N) * 4u))
+        return report_error(GBR_ERR_INVALID, "gemm_bias_relu_tf32_noalloc: C overlaps an input");
     if (!d->regs_ok)
         return report_error(GBR_ERR_CUDA, "tcgen05 GEMM kernel has too few registers for its role split");
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // Status words: zero at set-up and after every read that found a timeout,
+    // so a recorded timeout stays until gbr_device_status() reads it (the
+    // first one recorded is the one kept).  Bt: fully rewritten by the
+    // transpose of every call, so it needs no clearing.
     uint32_t* status = reinterpret_cast<uint32_t*>(d->scratch);
     float* bt = reinterpret_cast<float*>(d->scratch + kNoallocStatusBytes);
-    // The array keeps the last call's contents; the status words must start at zero.
-    if (cudaMemsetAsync(status, 0, kNoallocStatusBytes, st) != cudaSuccess)
-        return report_error(GBR_ERR_CUDA, "clearing the no-alloc status words failed");
 
     GemmShape s;
     memset(&s, 0, sizeof(s));
@@ -173,6 +204,7 @@ extern "C" int gemm_bias_relu_tf32_noalloc(const float* A, const float* B, const
     s.C = C;
     s.ctl.status = status;
     s.ctl.timeout_ns = wait_timeout_ns();
+    s.inject = injection_now();   // zero except under gbr_selftest_noalloc_skip_load
     s.m_tiles = int32_t((M + kUmmaBM - 1) / kUmmaBM);
     s.n_tiles = int32_t((N + kUmmaBN - 1) / kUmmaBN);
     s.num_kb = int32_t((K + 31) / 32);

@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(64, 1)
     // Every byte is read once and written once: optionally tell L2 to evict
     // these lines first, so they do not push out lines that will be reused.
     const bool hint_load = (a.l2_hint & 1u) != 0, hint_store = (a.l2_hint & 2u) != 0;
+    uint32_t issued = 0;   // load lane: ring items registered on full[]
     if (warp == 0 && lane == 0) {
         // ---------------- producer: wait empty -> expect_tx -> TMA load
         uint32_t i = 0, nt = 0;
@@ -73,12 +74,7 @@ __global__ void __launch_bounds__(64, 1)
         }
         trace_count(a.ctl, kRoleProducer, nt);
         ptx::griddep_launch_dependents();   // every load issued: the next launch may be scheduled
-        if (*abort_flag) {
-            // Let this CTA's own loads in flight land before the CTA exits.
-            const uint32_t n = i < uint32_t(S) ? i : uint32_t(S);
-            for (uint32_t j = i - n; j < i; ++j)
-                mbar_wait_drain(ptx::smem_addr(full + j % S), (j / S) & 1u, a.ctl.timeout_ns);
-        }
+        issued = i;
     } else if (warp == 1 && lane == 0) {
         // ---------------- storer: wait full -> TMA store -> release when read
         uint32_t i = 0, nt = 0;
@@ -111,6 +107,17 @@ __global__ void __launch_bounds__(64, 1)
         ptx::bulk_wait_group<0>();
     }
     __syncwarp();
+    __syncthreads();
+    // Both lanes have left their loops, so the abort flag is final.  After an
+    // abort the load lane lets its own loads still in flight land (the last S
+    // items it registered, except a self test's unissued one) before the CTA
+    // may exit.
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        const uint32_t n = issued < uint32_t(S) ? issued : uint32_t(S);
+        for (uint32_t j = issued - n; j < issued; ++j)
+            if (!inject_skip(a.inject, j))
+                mbar_wait_drain(ptx::smem_addr(full + j % S), (j / S) & 1u, a.ctl.timeout_ns);
+    }
     __syncthreads();
 }
 

@@ -84,3 +84,4 @@ class split_tail:
     def __exit__(self, *exc):
         self.gbr.gemm_split_tail(-1)
         return False
+

@@ -16,7 +16,7 @@ import torch
 
 import oracle
 from mbarrier_gemm_pipelines_gb300 import inputs
-from gpu_helpers import TOL, load_library, rel_frobenius, require_gpu, to_host_f64
+from gpu_helpers import TOL, load_library, rel_frobenius, require_gpu, to_host_f64, tuned
 
 pytestmark = pytest.mark.gpu
 
@@ -134,3 +134,46 @@ def test_repeated_injection_leaves_the_context_usable(gbr):
         gbr.selftest_gemm_skip_load(dA, dB, db, "bf16", 3, r % 4, r, LIMIT_NS)
         assert gbr.device_status() == 6
     _check_gemm(gbr, dA, dB, db, "bf16", 3)
+
+
+@pytest.mark.parametrize("dtype,stages,ks,unit,item", [
+    ("bf16", 3, 2, 0, 0), ("bf16", 3, 2, 3, 5), ("bf16", 6, 1, 1, 9), ("bf16", 6, 1, 2, 15),
+    ("tf32", 3, 2, 2, 3), ("tf32", 6, 1, 0, 11),
+])
+def test_pair_unfilled_stage_times_out_and_recovers(gbr, dtype, stages, ks, unit, item):
+    """The CTA-pair kernel (cta_group::2, the default tensor-core path): both
+    CTAs of pair `unit` leave ring item `item` unfilled.  The even CTA's MMA
+    lane (or an epilogue or producer wait of either CTA) gives up; the even
+    CTA then waits for every load either CTA issued, both free their Tensor
+    Memory and return.  512 x 512 x 1024: four 256 x 256 tiles, one per pair,
+    8 k-blocks of 128 K or 16 of 64 K each."""
+    A, B, bias = inputs.gemm_uniform(512, 512, 1024, seed=60 + item)
+    dev_dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    dA, dB, db = A.to(dev_dt).cuda(), B.to(dev_dt).cuda(), bias.cuda()
+    with tuned(gbr, 2, ks):
+        gbr.selftest_gemm_skip_load(dA, dB, db, dtype, stages, unit, item, LIMIT_NS)
+        code, msg = _status(gbr)
+        assert code == 6, msg
+        site, got_cta, got_item = _parse(msg)
+        assert got_cta in (2 * unit, 2 * unit + 1)
+        assert ((site, got_item) in ((SITE_MMA_FULL, item), (SITE_EPI_ACC_FULL, 0))
+                or _producer_gave_up(site, got_item, item, stages)), (hex(site), got_item)
+        assert gbr.device_status() == 0
+        _check_gemm(gbr, dA, dB, db, dtype, stages)
+
+
+def test_pair_repeated_injection_leaves_the_context_usable(gbr):
+    """Five timed-out CTA-pair launches in a row, alternating 128-K and 64-K
+    stages (both CTAs' Tensor Memory must be freed each time), then correct
+    GEMMs on the pair and on one CTA per tile."""
+    A, B, bias = inputs.gemm_uniform(512, 1024, 768, seed=51)
+    dA, dB, db = A.to(torch.bfloat16).cuda(), B.to(torch.bfloat16).cuda(), bias.cuda()
+    for r in range(5):
+        ks, S = (2, 3) if r % 2 == 0 else (1, 5)
+        with tuned(gbr, 2, ks):
+            gbr.selftest_gemm_skip_load(dA, dB, db, "bf16", S, r % 8, r + 1, LIMIT_NS)
+            assert gbr.device_status() == 6
+    with tuned(gbr, 2):
+        _check_gemm(gbr, dA, dB, db, "bf16", 3)
+    with tuned(gbr, 1):
+        _check_gemm(gbr, dA, dB, db, "bf16", 4)

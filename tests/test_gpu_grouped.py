@@ -1,5 +1,6 @@
 """Grouped (MoE-style) bf16 GEMM + bias + ReLU in one persistent launch against
-the oracle applied expert by expert.  Bar: relative Frobenius error 1e-2."""
+the oracle applied expert by expert, element by element over the whole output
+(the full-size MoE workload included).  Bar: relative Frobenius error 1e-2."""
 import numpy as np
 import pytest
 import torch
@@ -95,26 +96,34 @@ def test_grouped_rejects(gbr):
                                             bnd.BF16, 2, None) == bnd.ERR_INVALID
 
 
-@pytest.mark.parametrize("pair,S,ks", [(-1, 4, -1), (1, 4, -1), (2, 6, -1), (1, 2, 2), (2, 3, 2)])
-def test_config5_moe_sampled(gbr, pair, S, ks):
-    """4096 tokens over 8 experts (Multinomial counts, seed 4), K = 4096,
-    N = 14336, one launch; sampled positions in every expert."""
+@pytest.fixture(scope="module")
+def moe():
+    """The MoE workload (4096 tokens over 8 experts, Multinomial counts, seed
+    4, K = 4096, N = 14336) and its oracle output, with the biases and with
+    zero biases (the GEMM part alone), computed once for the module."""
     counts, X, W, b = inputs.workload("grouped_bf16")
-    with tuned(gbr, pair, ks):
-        C = gbr.gemm_bias_relu_grouped(X.cuda(), W.cuda(), b.cuda(), counts, stages=S)
-    gbr.check_device()
-    T, N = C.shape
-    rng = np.random.default_rng(4)
-    offs = oracle.group_offsets(counts)
-    rows, cols = [], []
-    for e, n_e in enumerate(counts):
-        if n_e == 0:
-            continue
-        r = offs[e] + rng.integers(0, n_e, 300)
-        rows += list(r) + [offs[e], offs[e] + n_e - 1]
-        cols += list(rng.integers(0, N, 300)) + [0, N - 1]
-    rows = np.array(rows, dtype=np.int64)
-    cols = np.array(cols, dtype=np.int64)
-    got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
-    ref = oracle.gemm_bias_relu_grouped_points(X.float(), W.float(), b, counts, rows, cols)
+    Xf, Wf = X.float(), W.float()
+    ref = oracle.gemm_bias_relu_grouped(Xf, Wf, b, counts)
+    ref0 = oracle.gemm_bias_relu_grouped(Xf, Wf, torch.zeros_like(b), counts)
+    return counts, X, W, b, ref, ref0
+
+
+def _check_moe(got, ref):
     assert rel_frobenius(got, ref) <= TOL["bf16"]
+    assert (got >= 0).all()
+    assert np.abs(got - ref).max() <= 20 * TOL["bf16"] * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("pair,S,ks", [(-1, 4, -1), (1, 4, -1), (2, 6, -1), (1, 2, 2), (2, 3, 2),
+                                        (-1, 3, -1)])
+def test_config5_moe(gbr, moe, pair, S, ks):
+    """One launch over all experts' tiles; every output element of every
+    expert against the oracle, with the biases and without them."""
+    counts, X, W, b, ref, ref0 = moe
+    dX, dW, db = X.cuda(), W.cuda(), b.cuda()
+    with tuned(gbr, pair, ks):
+        C = gbr.gemm_bias_relu_grouped(dX, dW, db, counts, stages=S)
+        C0 = gbr.gemm_bias_relu_grouped(dX, dW, torch.zeros_like(db), counts, stages=S)
+    gbr.check_device()
+    _check_moe(to_host_f64(C), ref)
+    _check_moe(to_host_f64(C0), ref0)

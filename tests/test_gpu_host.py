@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from mbarrier_gemm_pipelines_gb300 import inputs
-from gpu_helpers import (TOL, load_library, rel_frobenius, require_gpu, sample_points, split_tail,
+from gpu_helpers import (TOL, load_library, rel_frobenius, require_gpu, split_tail,
                          to_host_f64)
 
 pytestmark = pytest.mark.gpu
@@ -51,16 +51,16 @@ def test_host_pageable_inputs(gbr):
     assert rel_frobenius(to_host_f64(C), ref) <= TOL["bf16"]
 
 
-def test_host_eight_chunks_sampled(gbr):
-    """8192 rows: eight 1024-row chunks in flight at once (split tail on)."""
+def test_host_eight_chunks(gbr):
+    """8192 rows: eight 1024-row chunks in flight at once; every element."""
     M, N, K = 8192, 1024, 1024
     A, B, bias = _host_inputs(M, N, K, "bf16", seed=9)
     C = gbr.gemm_bias_relu_host(A, B, bias, dtype="bf16", stages=3)
     gbr.check_device()
-    ms, ns = sample_points(M, N, 2000, seed=9, extra_rows=(0, 1023, 1024, 4095, 7168, M - 1))
-    got = C[torch.from_numpy(ms), torch.from_numpy(ns)].double().numpy()
-    ref = oracle.gemm_bias_relu_points(A.float(), B.float(), bias, ms, ns)
+    ref = oracle.gemm_bias_relu(A.float(), B.float(), bias)
+    got = to_host_f64(C)
     assert rel_frobenius(got, ref) <= TOL["bf16"]
+    assert np.abs(got - ref).max() <= 20 * TOL["bf16"] * np.abs(ref).max()
 
 
 def test_host_k_zero_and_empty(gbr):

@@ -2,18 +2,17 @@
 cannot allocate device memory (serving loops that must stay out of allocators,
 plug-ins whose host framework owns device allocation, processes whose device
 memory is reserved by another allocator).  Its scratch is a fixed device array
-inside the library, so its output must match the regular entry point's,
-call after call, although every call reuses the same array.
+inside the library that every call on the device reuses, so its output is
+checked against the binary64 oracle call after call, at the TF32 bar.
 
 Collected last (file name) so that a run stopping at the first failure has
 already run every other test; it also passes on its own in a fresh process,
 where its first call is the library's first call on the device."""
-import ctypes
-
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from mbarrier_gemm_pipelines_gb300 import inputs
 from gpu_helpers import TOL, load_library, rel_frobenius, require_gpu, to_host_f64
 
@@ -21,6 +20,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _noalloc(lib, A, B, bias, C, stages):
+    """The raw C-ABI call, with the sizes taken from A and B."""
     M, K = A.shape
     N = B.shape[1]
     return lib.gemm_bias_relu_tf32_noalloc(A.data_ptr(), B.data_ptr(), bias.data_ptr(),
@@ -28,24 +28,27 @@ def _noalloc(lib, A, B, bias, C, stages):
                                            torch.cuda.current_stream().cuda_stream)
 
 
-def test_noalloc_matches_regular_entry_point_twice():
+def _check_oracle(C, A, B, bias):
+    got = to_host_f64(C)
+    ref = oracle.gemm_bias_relu(A, B, bias)
+    assert np.isfinite(got).all()
+    assert rel_frobenius(got, ref) <= TOL["tf32"]
+    assert np.abs(got - ref).max() <= 20 * TOL["tf32"] * (np.abs(ref).max() + 1e-30)
+
+
+def test_noalloc_matches_oracle_twice():
     require_gpu()
     gbr = load_library()
     from mbarrier_gemm_pipelines_gb300 import _binding as b
     lib = b.lib()
     # Two calls in a row with different shapes: the second reuses the scratch
-    # array the first one left behind.
-    for M, N, K, seed in [(300, 520, 200, 21), (640, 1024, 2048, 22)]:
+    # array the first one left behind (a larger K-major B copy, then a smaller one).
+    for M, N, K, seed in [(640, 1024, 2048, 22), (300, 520, 200, 21)]:
         A, B, bias = inputs.gemm_normal(M, N, K, seed=seed)
-        dA, dB, dbias = A.cuda(), B.cuda(), bias.cuda()
         C = torch.full((M, N), float("nan"), device="cuda")
-        assert _noalloc(lib, dA, dB, dbias, C, 3) == b.OK, b.last_error()
+        assert _noalloc(lib, A.cuda(), B.cuda(), bias.cuda(), C, 3) == b.OK, b.last_error()
         gbr.check_device()
-        ref = gbr.gemm_bias_relu(dA, dB, dbias, dtype="tf32", stages=3)
-        gbr.check_device()
-        got, want = to_host_f64(C), to_host_f64(ref)
-        assert np.isfinite(got).all()
-        assert rel_frobenius(got, want) <= TOL["tf32"]
+        _check_oracle(C, A, B, bias)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
@@ -62,3 +65,67 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     assert _noalloc(lib, A, B, bias, C, 3) == b.ERR_INVALID
     assert "16 MiB" in b.last_error()
     assert lib.gbr_launch_count() == before
+
+
+def test_noalloc_rejects_overlap_and_deep_rings():
+    require_gpu()
+    gbr = load_library()
+    from mbarrier_gemm_pipelines_gb300 import _binding as b
+    lib = b.lib()
+    A, B, bias = inputs.gemm_normal(256, 256, 256, seed=23)
+    dA, dB, db = A.cuda(), B.cuda(), bias.cuda()
+    C = torch.empty((256, 256), device="cuda")
+    before = lib.gbr_launch_count()
+    assert _noalloc(lib, dA, dB, db, dA, 3) == b.ERR_INVALID      # C is A
+    assert "overlap" in b.last_error()
+    assert _noalloc(lib, dA, dB, db, dB, 3) == b.ERR_INVALID      # C is B
+    # One CTA per tile: 4 stages at most, although the pair kernel holds more.
+    assert gbr.max_stages(gbr.OP_GEMM, gbr.F32_TF32) > 4
+    assert _noalloc(lib, dA, dB, db, C, 5) == b.ERR_SMEM
+    assert "[1, 4]" in b.last_error()
+    assert _noalloc(lib, dA, dB, db, C, 0) == b.ERR_SMEM
+    assert lib.gbr_launch_count() == before
+    assert _noalloc(lib, dA, dB, db, C, 4) == b.OK
+    gbr.check_device()
+    _check_oracle(C, A, B, bias)
+
+
+def test_noalloc_python_wrapper_checks_shapes():
+    require_gpu()
+    gbr = load_library()
+    A = torch.zeros((64, 32), device="cuda")
+    B = torch.zeros((32, 96), device="cuda")
+    bias = torch.zeros(96, device="cuda")
+    before = gbr.launch_count()
+    for args in ((A, B, bias, torch.zeros((64, 64), device="cuda")),       # C too narrow
+                 (A, torch.zeros((40, 96), device="cuda"), bias,           # K mismatch
+                  torch.zeros((64, 96), device="cuda")),
+                 (A, B, torch.zeros(64, device="cuda"),                    # bias length
+                  torch.zeros((64, 96), device="cuda"))):
+        with pytest.raises(ValueError):
+            gbr.gemm_bias_relu_tf32_noalloc(*args, stages=3)
+    with pytest.raises(TypeError):
+        gbr.gemm_bias_relu_tf32_noalloc(A, B, bias, torch.zeros((64, 96), device="cuda",
+                                                                dtype=torch.bfloat16))
+    assert gbr.launch_count() == before
+
+
+def test_noalloc_timeout_is_reported_then_cleared():
+    """A stage left unfilled on the host's instruction (50 ms limit): the
+    kernel gives up, records the timeout in the no-alloc array's status words
+    and returns; gbr_device_status reports it once, and the next call is
+    correct again."""
+    require_gpu()
+    gbr = load_library()
+    A, B, bias = inputs.gemm_normal(384, 512, 640, seed=24)
+    dA, dB, db = A.cuda(), B.cuda(), bias.cuda()
+    C = torch.empty((384, 512), device="cuda")
+    gbr.selftest_noalloc_skip_load(dA, dB, db, C, stages=3, cta=1, item=2,
+                                   limit_ns=50_000_000)
+    assert gbr.device_status() == 6                    # GBR_ERR_TIMEOUT
+    msg = gbr.last_error()
+    assert "gemm_bias_relu_tf32_noalloc" in msg and "CTA 1" in msg
+    assert gbr.device_status() == 0                    # read once, then cleared
+    gbr.gemm_bias_relu_tf32_noalloc(dA, dB, db, C, stages=3)
+    gbr.check_device()
+    _check_oracle(C, A, B, bias)
