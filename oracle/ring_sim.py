@@ -420,3 +420,136 @@ def simulate_gemm(n_tiles: int, k_blocks: int, stages: int, acc_slots: int = 2,
     agents = [_Agent("producer", producer()), _Agent("mma", mma())]
     agents += [_Agent("epi%d" % w, epilogue(w)) for w in range(epi_warps)]
     return _run(agents, [tma, tc], rng, max_steps, trace)
+
+
+# ---------------------------------------------------------------------------
+# Replay of an event trace recorded on the GPU.
+#
+# A trace event is a tuple (t, ev, item, slot, parity): t a timestamp, ev one
+# of "wait" (a wait returned; recorded after it), "issued" (a producer issued
+# an item's copies, or the MMA lane committed a tile to its accumulator;
+# recorded before) or "released" (a consumer released a slot; recorded
+# before).  Events are replayed in time order, with "issued"/"released"
+# before "wait" at equal times, through the MBarrier model above:
+#
+# * a producer's "issued" registers the item on full[slot] (the first
+#   producer of a unit registers every producer's bytes, as one arrive with
+#   expect-tx) and puts its copy in flight;
+# * a consumer's "wait" on full first lands the item's copies in flight, then
+#   must find the phase it names complete (I4); its item must be the one the
+#   slot holds and every producer must have issued it (I2);
+# * a "released" arrives on empty[slot] of every producer (on the CTA pair the
+#   commit reaches both CTAs' empty barriers); a producer's "wait" on empty
+#   must find its phase complete, which is what keeps a slot from being
+#   refilled before it was released (I1);
+# * the accumulator ring likewise: the MMA lane waits on acc_empty and
+#   commits to every epilogue role's acc_full; each epilogue role waits on its
+#   acc_full and arrives on acc_empty.
+#
+# Slot and parity of every wait must also follow ``rules``.
+
+def replay(producers, consumer, stages: int, mma_acc=None, epilogues=None,
+           rules: Rules = Rules(), acc_slots: int = 2) -> Trace:
+    """Replays one unit's GPU trace; raises Violation at the first event the
+    model contradicts.  producers: one event list per producing CTA;
+    consumer: the consuming role's events; mma_acc / epilogues: the
+    accumulator ring's events (optional)."""
+    S, P = stages, len(producers)
+    if P < 1:
+        raise ValueError("need at least one producer")
+    full = [MBarrier(1, "full%d" % s) for s in range(S)]
+    empty = [[MBarrier(1, "empty%d.%d" % (p, s)) for s in range(S)] for p in range(P)]
+    holds = [None] * S              # item the slot was last registered for
+    issuers = [set() for _ in range(S)]
+    in_flight = {}                  # item -> producers whose copy has not landed
+    trace = Trace()
+    stream = []
+    kinds = {"issued": 0, "released": 0, "wait": 1}
+    for p, evs in enumerate(producers):
+        stream += [(t, kinds[ev], "producer", p, ev, i, s, par) for (t, ev, i, s, par) in evs]
+    stream += [(t, kinds[ev], "consumer", 0, ev, i, s, par) for (t, ev, i, s, par) in consumer]
+    E = len(epilogues or [])
+    if mma_acc is not None:
+        acc_full = [[MBarrier(1, "acc_full%d.%d" % (e, a)) for a in range(acc_slots)]
+                    for e in range(E)]
+        acc_empty = [MBarrier(E, "acc_empty%d" % a) for a in range(acc_slots)]
+        committed = {}              # accumulator item -> epilogue roles not yet signalled
+        stream += [(t, kinds[ev], "mma_acc", 0, ev, i, s, par) for (t, ev, i, s, par) in mma_acc]
+        for e, evs in enumerate(epilogues):
+            stream += [(t, kinds[ev], "epilogue", e, ev, i, s, par) for (t, ev, i, s, par) in evs]
+    stream.sort(key=lambda x: (x[0], x[1]))
+
+    for t, _, role, who, ev, i, s, par in stream:
+        trace.steps += 1
+        if role == "producer":
+            if s != rules.slot(i, S):
+                raise Violation("producer %d: item %d in slot %d" % (who, i, s))
+            if ev == "wait":
+                if par != rules.empty_parity(i, S):
+                    raise Violation("producer %d: item %d waited empty parity %d" % (who, i, par))
+                if not empty[who][s].test_wait_parity(par):
+                    raise Violation("I1/I4: producer %d passed empty[%d] (parity %d) for item %d "
+                                    "before the slot's previous item was released" % (who, s, par, i))
+                trace.events.append(Event("producer%d" % who, "empty_ok", i, s, par,
+                                          empty[who][s].completed))
+            elif ev == "issued":
+                if holds[s] != i:
+                    if holds[s] is not None and issuers[s] and holds[s] in in_flight:
+                        raise Violation("I1: item %d issued into slot %d while item %d is still "
+                                        "in flight" % (i, s, holds[s]))
+                    if full[s].completed != i // S:
+                        raise Violation("I1: item %d issued into slot %d in phase %d"
+                                        % (i, s, full[s].completed))
+                    holds[s], issuers[s] = i, set()
+                    full[s].arrive_expect_tx(P)     # one unit of bytes per producer's copy
+                issuers[s].add(who)
+                in_flight.setdefault(i, set()).add(who)
+                trace.events.append(Event("producer%d" % who, "issue", i, s))
+        elif role == "consumer":
+            if s != rules.slot(i, S):
+                raise Violation("consumer: item %d in slot %d" % (i, s))
+            if ev == "wait":
+                if par != rules.full_parity(i, S):
+                    raise Violation("consumer: item %d waited full parity %d" % (i, par))
+                if holds[s] != i or len(issuers[s]) != P:
+                    raise Violation("I2: consumer passed full[%d] for item %d, which holds item %s "
+                                    "issued by %d of %d producers"
+                                    % (s, i, holds[s], len(issuers[s]), P))
+                for _ in in_flight.pop(i, set()):
+                    full[s].complete_tx(1)
+                if not full[s].test_wait_parity(par):
+                    raise Violation("I4: consumer passed full[%d] (parity %d) for item %d before "
+                                    "the phase completed" % (s, par, i))
+                trace.events.append(Event("consumer", "full_ok", i, s, par, full[s].completed))
+            elif ev == "released":
+                if holds[s] != i:
+                    raise Violation("consumer released slot %d for item %d, which holds item %s"
+                                    % (s, i, holds[s]))
+                for p in range(P):
+                    empty[p][s].arrive()
+                trace.events.append(Event("consumer", "release", i, s))
+        elif role == "mma_acc":
+            if s != i % acc_slots:
+                raise Violation("MMA lane: accumulator item %d in slot %d" % (i, s))
+            if ev == "wait":
+                want = ((i // acc_slots) & 1) ^ 1
+                if par != want or not acc_empty[s].test_wait_parity(par):
+                    raise Violation("MMA lane passed acc_empty[%d] (parity %d) for item %d before "
+                                    "the epilogue released it" % (s, par, i))
+            elif ev == "issued":
+                committed[i] = set(range(E))
+        else:   # epilogue role `who`
+            if s != i % acc_slots:
+                raise Violation("epilogue %d: accumulator item %d in slot %d" % (who, i, s))
+            if ev == "wait":
+                if par != (i // acc_slots) & 1:
+                    raise Violation("epilogue %d: item %d waited parity %d" % (who, i, par))
+                if who in committed.get(i, ()):
+                    committed[i].discard(who)
+                    acc_full[who][s].arrive()
+                if not acc_full[who][s].test_wait_parity(par):
+                    raise Violation("epilogue %d passed acc_full[%d] for item %d before its commit"
+                                    % (who, s, i))
+            elif ev == "released":
+                acc_empty[s].arrive()
+    return trace

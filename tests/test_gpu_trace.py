@@ -7,12 +7,42 @@ import pytest
 import torch
 
 import oracle
+from oracle import ring_sim
 from mbarrier_gemm_pipelines_gb300 import inputs, trace
 from gpu_helpers import (TOL, load_library, rel_frobenius, require_gpu, split_tail, to_host_f64,
                          tuned)
+import trace_check as roles
 from trace_check import check
 
 pytestmark = pytest.mark.gpu
+
+EVENT_KIND = {trace.WAIT_DONE: "wait", trace.ISSUED: "issued", trace.RELEASED: "released"}
+
+
+def _tuples(recs):
+    return [(int(r["t"]), EVENT_KIND[int(r["ev"])], int(r["item"]), int(r["slot"]),
+             int(r["parity"])) for r in recs]
+
+
+def replay_units(ev, S, cta_group=1, accumulator=False):
+    """Replays every unit's recorded events through the ring simulator's
+    mbarrier model (it raises at the first contradiction); returns the
+    number of units replayed."""
+    n = 0
+    for u in sorted({cta // cta_group for cta, _ in ev}):
+        lead = u * cta_group
+        if (lead, roles.CONSUMER) not in ev:
+            continue
+        members = range(lead, lead + cta_group)
+        prods = [_tuples(ev[(c, roles.PRODUCER)]) for c in members]
+        cons = _tuples(ev[(lead, roles.CONSUMER)])
+        mma = epis = None
+        if accumulator:
+            mma = _tuples(ev[(lead, roles.MMA_ACC)])
+            epis = [_tuples(ev[(c, roles.EPILOGUE)]) for c in members]
+        ring_sim.replay(prods, cons, S, mma_acc=mma, epilogues=epis)
+        n += 1
+    return n
 
 
 @pytest.fixture(scope="module")
@@ -36,6 +66,7 @@ def test_copy_trace(gbr, S, lag):
     assert len(ev) >= 2 * 100
     errs = check(ev, cnt, S)
     assert errs == [], errs[:5]
+    assert replay_units(ev, S) >= 100
 
 
 @pytest.mark.parametrize("dtype", ["ffma", "ffma_cpasync"])
@@ -49,6 +80,7 @@ def test_ffma_trace(gbr, dtype, S):
     assert rel_frobenius(to_host_f64(C), oracle.gemm_bias_relu(A, B, bias)) <= TOL[dtype]
     errs = check(ev, cnt, S)
     assert errs == [], errs[:5]
+    assert replay_units(ev, S) >= 16
 
 
 @pytest.mark.parametrize("dtype,pair,ks,S,split", [
@@ -71,6 +103,7 @@ def test_umma_trace(gbr, dtype, pair, ks, S, split):
     assert rel_frobenius(to_host_f64(C), ref) <= TOL[dtype]
     errs = check(ev, cnt, S, cta_group=pair, accumulator=True)
     assert errs == [], errs[:5]
+    assert replay_units(ev, S, cta_group=pair, accumulator=True) >= 64 // pair
 
 
 def test_umma_trace_many_tiles_per_unit(gbr):
@@ -86,6 +119,7 @@ def test_umma_trace_many_tiles_per_unit(gbr):
     errs = check(ev, cnt, 3, cta_group=2, accumulator=True)
     assert errs == [], errs[:5]
     assert max(len(v) for (cta, role), v in ev.items() if role == 2) >= 6   # >= 3 tiles
+    assert replay_units(ev, 3, cta_group=2, accumulator=True) == 76
 
 
 @pytest.mark.parametrize("pair", [1, 2])
@@ -100,6 +134,7 @@ def test_grouped_trace(gbr, pair):
     assert rel_frobenius(to_host_f64(C), ref) <= TOL["bf16"]
     errs = check(ev, cnt, 3, cta_group=pair, accumulator=True)
     assert errs == [], errs[:5]
+    assert replay_units(ev, 3, cta_group=pair, accumulator=True) >= 1
 
 
 def test_trace_off_leaves_buffer_untouched(gbr):

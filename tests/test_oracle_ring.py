@@ -175,3 +175,112 @@ def test_property_ring(S, n, c, seed):
        acc=st.integers(1, 3), seed=st.integers(0, 2 ** 31 - 1))
 def test_property_gemm(S, tiles, kb, acc, seed):
     rs.simulate_gemm(tiles, kb, S, acc_slots=acc, seed=seed)
+
+
+# ------------------------------------------------------------------ replay
+# The replay entry point feeds a recorded event trace through the same
+# mbarrier model.  A run of the simulator, written out as such a trace, must
+# replay cleanly; each planted mistake must be reported.
+
+def _as_trace(tr):
+    """The simulator's own events as a replay input (list order = time)."""
+    prod, cons = [], []
+    for t, e in enumerate(tr.events):
+        if e.agent == "producer":
+            prod.append((t, "wait" if e.what == "empty_ok" else "issued", e.item, e.slot,
+                         e.parity or 0))
+        elif e.what == "full_ok":
+            cons.append((t, "wait", e.item, e.slot, e.parity))
+        elif e.what == "release":
+            cons.append((t, "released", e.item, e.slot, 0))
+    return prod, cons
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 5])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_replay_of_a_simulated_run_passes(S, seed):
+    tr = rs.simulate_ring(23, S, seed=seed)
+    prod, cons = _as_trace(tr)
+    assert len(prod) == 2 * 23 and len(cons) == 2 * 23
+    rep = rs.replay([prod], cons, S)
+    assert len(rep.of("consumer", "full_ok")) == 23
+
+
+def _unit(n, S, pair=False, tiles_k=4):
+    """A valid trace of one unit: item i is issued once item i - S is released;
+    tiles of tiles_k items go through a two-slot accumulator ring read by one
+    epilogue role per CTA."""
+    P = 2 if pair else 1
+    prods = [[] for _ in range(P)]
+    cons, mma, epis = [], [], [[] for _ in range(P)]
+    t = 0
+    for i in range(n):
+        t += 10
+        for p in range(P):
+            prods[p] += [(t, "wait", i, i % S, ((i // S) & 1) ^ 1), (t + 1, "issued", i, i % S, 0)]
+        cons += [(t + 5, "wait", i, i % S, (i // S) & 1), (t + 6, "released", i, i % S, 0)]
+        if i % tiles_k == tiles_k - 1:
+            tl = i // tiles_k
+            mma += [(t + 2, "wait", tl, tl % 2, ((tl // 2) & 1) ^ 1), (t + 7, "issued", tl, tl % 2, 0)]
+            for e in range(P):
+                epis[e] += [(t + 8, "wait", tl, tl % 2, (tl // 2) & 1), (t + 9, "released", tl, tl % 2, 0)]
+    return prods, cons, mma, epis
+
+
+@pytest.mark.parametrize("S,pair", [(1, False), (2, False), (4, False), (3, True), (6, True)])
+def test_replay_of_a_valid_unit_passes(S, pair):
+    prods, cons, mma, epis = _unit(24, S, pair)
+    rs.replay(prods, cons, S, mma_acc=mma, epilogues=epis)
+
+
+def test_replay_reports_a_refill_before_release():
+    prods, cons, mma, epis = _unit(12, 2)
+    # the release of item 3 moves after the producer's wait for item 5
+    k = [j for j, ev in enumerate(cons) if ev[1] == "released" and ev[2] == 3][0]
+    wait5 = [ev for ev in prods[0] if ev[1] == "wait" and ev[2] == 5][0]
+    cons[k] = (wait5[0] + 3,) + cons[k][1:]
+    cons.sort()
+    with pytest.raises(rs.Violation, match="before the slot's previous item was released"):
+        rs.replay(prods, cons, 2)
+
+
+def test_replay_reports_a_wrong_parity():
+    prods, cons, _, _ = _unit(8, 2)
+    k = [j for j, ev in enumerate(cons) if ev[1] == "wait" and ev[2] == 3][0]
+    cons[k] = cons[k][:4] + (0,)                 # item 3 must wait on parity 1
+    with pytest.raises(rs.Violation, match="parity"):
+        rs.replay(prods, cons, 2)
+
+
+def test_replay_reports_a_stage_seen_before_the_peer_issued_it():
+    prods, cons, _, _ = _unit(8, 3, pair=True)
+    prods[1] = [ev for ev in prods[1] if not (ev[1] == "issued" and ev[2] == 4)]
+    with pytest.raises(rs.Violation, match="I2"):
+        rs.replay(prods, cons, 3)
+
+
+def test_replay_reports_a_wrong_slot():
+    prods, cons, _, _ = _unit(8, 3)
+    k = [j for j, ev in enumerate(prods[0]) if ev[1] == "issued" and ev[2] == 4][0]
+    prods[0][k] = prods[0][k][:3] + (0, 0)
+    with pytest.raises(rs.Violation, match="slot"):
+        rs.replay(prods, cons, 3)
+
+
+def test_replay_reports_an_accumulator_read_before_its_commit():
+    prods, cons, mma, epis = _unit(16, 2)
+    k = [j for j, ev in enumerate(mma) if ev[1] == "issued" and ev[2] == 1][0]
+    w = [ev for ev in epis[0] if ev[1] == "wait" and ev[2] == 1][0]
+    mma[k] = (w[0] + 1,) + mma[k][1:]
+    with pytest.raises(rs.Violation, match="before its commit"):
+        rs.replay(prods, cons, 2, mma_acc=mma, epilogues=epis)
+
+
+def test_replay_reports_an_accumulator_reused_before_release():
+    prods, cons, mma, epis = _unit(24, 2, pair=True)
+    # tile 0's release by the odd CTA's epilogue comes after the MMA lane's wait for tile 2
+    w2 = [ev for ev in mma if ev[1] == "wait" and ev[2] == 2][0]
+    k = [j for j, ev in enumerate(epis[1]) if ev[1] == "released" and ev[2] == 0][0]
+    epis[1][k] = (w2[0] + 1,) + epis[1][k][1:]
+    with pytest.raises(rs.Violation, match="before the epilogue released it"):
+        rs.replay(prods, cons, 2, mma_acc=mma, epilogues=epis)
