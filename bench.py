@@ -366,6 +366,15 @@ def measure_workloads(gbr, peaks, sm_mhz=None, steps=20, warmup=3):
             "value": round(v, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
             "roofline": {"bound": "alu", "achieved": round(v, 2), "peak": round(fp32_alu_peak, 1),
                          "unit": "TFLOP/s", "frac": round(v / fp32_alu_peak, 4)}}
+    # The 16-warp consumer layout (8x4 micro-tiles, 4 consumer warps per
+    # scheduler) beside the default 8-warp one.
+    gbr.ffma_tuning(16)
+    v, ms = timed(lambda: gbr.gemm_bias_relu(dA, dB, db, dC, dtype="ffma", stages=4), f)
+    gbr.ffma_tuning(-1)
+    out["gemm_fp32_4096_ffma_16warps_S4"] = {
+        "value": round(v, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
+        "roofline": {"bound": "alu", "achieved": round(v, 2), "peak": round(fp32_alu_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(v / fp32_alu_peak, 4)}}
     # The historical producer: the same ring and consumers, fed by a cp.async
     # warpgroup instead of one TMA lane.
     for S in (2, 4):
@@ -390,6 +399,14 @@ def measure_workloads(gbr, peaks, sm_mhz=None, steps=20, warmup=3):
     v, ms = timed(lambda: gbr.gemm_bias_relu_grouped(dX, dW, db, counts, dC, stages=3), f)
     out["grouped_bf16_moe_S3"] = {
         "value": round(v, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4), "counts": counts,
+        "roofline": {"bound": "tensor", "achieved": round(v, 2), "peak": bf16_peak,
+                     "unit": "TFLOP/s", "frac": round(v / bf16_peak, 4)}}
+    # The same with every expert's last tile padded to 256 rows (thin tails off).
+    gbr.gemm_thin_tail(False)
+    v, ms = timed(lambda: gbr.gemm_bias_relu_grouped(dX, dW, db, counts, dC, stages=3), f)
+    gbr.gemm_thin_tail(True)
+    out["grouped_bf16_moe_S3_no_thin"] = {
+        "value": round(v, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
         "roofline": {"bound": "tensor", "achieved": round(v, 2), "peak": bf16_peak,
                      "unit": "TFLOP/s", "frac": round(v / bf16_peak, 4)}}
     del dX, dW, db, dC

@@ -247,6 +247,43 @@ int gbr_gemm_split_tail(int mode);
 int gbr_gemm_dynamic_schedule(int on);
 
 /*
+ * Tile order of the dense tensor-core GEMM, for all later calls in the
+ * process.  band_cols 0 (default): bands of gbr_gemm_tuning's group_m tile
+ * rows, column-major inside a band.  band_cols > 0: bands of band_cols tile
+ * columns, row-major inside a band, so that the units running at once share
+ * the band's B column strips while A rows stream past.  Every tile adds the
+ * same products either way; only the order of tiles, and so L2 reuse,
+ * changes.  GBR_ERR_INVALID for a negative value.
+ */
+int gbr_gemm_raster_cols(int band_cols);
+
+/*
+ * Consumer layout of the strict-fp32 FFMA GEMM (GBR_F32_FFMA, its cp.async
+ * variant and the homogeneous baseline's micro-tile), for all later calls in
+ * the process.  consumer_warps 8 (-1: the default): 8 consumer warps (2 per
+ * warp scheduler) of an 8 x 8 register micro-tile each per 128 x 128 output
+ * tile, 384 threads per CTA.  16: 16 consumer warps (4 per scheduler) of
+ * 8 x 4, 640 threads per CTA (more warps, but more shared-memory reads per
+ * FMA: measured slower).  Results are the same bits either way (each output
+ * adds the same products in the same order).  GBR_ERR_INVALID for other
+ * values.
+ */
+int gbr_ffma_tuning(int consumer_warps);
+
+/*
+ * Thin tail tiles of gemm_bias_relu_grouped on the CTA pair, for all later
+ * calls in the process.  on = 1 (default): an expert's last M-tile with at
+ * most 128 rows (t rows) is computed transposed, C^T = W^T X^T, as one
+ * M = 256 x N = t rounded up to 16 tcgen05 MMA per K step (the weight panels
+ * read as an MN-major A operand, the rows as a K-major B operand), and its
+ * epilogue writes the tile column by column; the MMA work of such a tile
+ * shrinks from 256 rows to t (rounded up to 16).  The split tail is off in
+ * launches with thin tiles.  on = 0: every tile is a 256-row tile.  Results
+ * agree to fp32 accumulation order.  GBR_ERR_INVALID for other values.
+ */
+int gbr_gemm_thin_tail(int on);
+
+/*
  * Programmatic dependent launch of the library's pipeline kernels (the
  * staged copy, the FFMA and tensor-core GEMMs and the TF32 B transpose), for
  * all later calls in the process.  on = 1 (default): each is launched so that

@@ -40,6 +40,9 @@ SIGNATURES = {
     "gbr_gemm_split_tail": (_i32, [_i32]),
     "gbr_gemm_dynamic_schedule": (_i32, [_i32]),
     "gbr_launch_overlap": (_i32, [_i32]),
+    "gbr_gemm_thin_tail": (_i32, [_i32]),
+    "gbr_ffma_tuning": (_i32, [_i32]),
+    "gbr_gemm_raster_cols": (_i32, [_i32]),
     "gbr_trace_buffer": (_i32, [_vp, _u64]),
     "gbr_selftest_wait_timeout": (_i32, [_u64, _vp]),
     "gbr_selftest_gemm_skip_load": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32,
@@ -259,6 +262,22 @@ def gemm_split_tail(mode: int = -1) -> None:
 def gemm_dynamic_schedule(on: bool) -> None:
     """Tensor-core GEMM tiles from an atomic counter (True) or the static order (see gbr.h)."""
     check(lib().gbr_gemm_dynamic_schedule(int(bool(on))))
+
+
+def gemm_raster_cols(band_cols: int = 0) -> None:
+    """Dense tensor-core tile order: 0 row bands (default), n > 0 bands of n tile columns (see gbr.h)."""
+    check(lib().gbr_gemm_raster_cols(int(band_cols)))
+
+
+def ffma_tuning(consumer_warps: int = -1) -> None:
+    """FFMA GEMM consumer layout: 8 warps of 8x8 (-1, default) or 16 warps of 8x4 (see gbr.h)."""
+    check(lib().gbr_ffma_tuning(int(consumer_warps)))
+
+
+def gemm_thin_tail(on: bool) -> None:
+    """Grouped CTA-pair launches: run experts' last M-tiles of <= 128 rows
+    transposed (True, default) or as 256-row tiles (False) (see gbr.h)."""
+    check(lib().gbr_gemm_thin_tail(int(bool(on))))
 
 
 def launch_overlap(on: bool) -> None:

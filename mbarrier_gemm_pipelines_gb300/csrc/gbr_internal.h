@@ -73,6 +73,8 @@ struct GemmShape {
     int32_t num_tiles;
     int32_t stages;
     int32_t group_m;
+    int32_t group_n;               // tensor-core dense: > 0 bands of group_n tile columns
+                                   // (row-major inside), instead of group_m-row bands
     const float* bias;
     void* C;                       // used by epilogues that store with st.global
     const void* A;                 // read directly only by the cp.async producer variant
@@ -111,6 +113,10 @@ cudaError_t ffma_occupancy(size_t smem, int* blocks_per_sm);
 cudaError_t ffma_check_registers(int* regs);
 cudaError_t launch_gemm_ffma(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmShape& s,
                              int grid, size_t smem, cudaStream_t stream, bool cpasync = false);
+// Consumer warps of the FFMA kernels (and of the homogeneous baseline's
+// micro-tile layout): 16 (default) or 8; returns 0, or -1 for other values.
+int ffma_set_consumer_warps(int cw);
+int ffma_consumer_warps();
 // Homogeneous baseline (every thread loads, syncs, computes, syncs); one CTA
 // per 128x128 tile, single-buffered, plain global loads.
 cudaError_t launch_gemm_ffma_sync(const float* A, const float* B, const GemmShape& s,
@@ -122,6 +128,9 @@ constexpr uint32_t kUmmaAStageBytes = kUmmaBM * 128;        // 16 KiB
 constexpr uint32_t kUmmaBStageBytes = kUmmaBN * 128;        // 32 KiB
 constexpr uint32_t kUmmaStageBytes = kUmmaAStageBytes + kUmmaBStageBytes;
 constexpr uint32_t kUmmaEpiBytes = 4 * 2 * 32 * 128;        // 4 warps x 2 buffers x 4 KiB
+// Barriers and small per-CTA words after the epilogue staging: 20 S + 132
+// bytes for S ring stages (S <= 6 on every kernel instance), rounded up.
+constexpr uint32_t kUmmaBarrierBytes = 384;
 constexpr int kMaxGroups = 32;
 
 // bf16 (B read MN-major from B[K, N]); TF32 (B read K-major from a transposed
@@ -135,6 +144,10 @@ struct GroupTable {
     int32_t rows[kMaxGroups];          // n_e
     int32_t m_tiles[kMaxGroups];       // ceil(n_e / tile rows)
     int32_t tile_start[kMaxGroups + 1];  // prefix sum of m_tiles[e] * n_tiles
+    // CTA-pair launches: rows of group e's last M-tile when that tile runs
+    // transposed (a "thin" tile: C^T = W^T X^T, the tile's rows as the MMA's
+    // N), or 0 when it runs as an ordinary 256-row tile.
+    int32_t thin[kMaxGroups];
 };
 
 // pair = 1: one CTA per 128x256 tile; pair = 2: a two-CTA cluster per 256x256
@@ -152,7 +165,9 @@ cudaError_t launch_gemm_umma(int kind, int pair, const CUtensorMap& mapA, const 
 cudaError_t launch_gemm_umma(int kind, const CUtensorMap& mapA, const CUtensorMap& mapB,
                              const CUtensorMap& mapC, const GemmShape& s, int grid, size_t smem,
                              cudaStream_t stream);
-cudaError_t launch_gemm_umma_grouped(int pair, const CUtensorMap& mapX, const CUtensorMap& mapW,
+// mapX_thin: X in boxes of 16 rows, read by thin tiles (GroupTable::thin).
+cudaError_t launch_gemm_umma_grouped(int pair, const CUtensorMap& mapX,
+                                     const CUtensorMap& mapX_thin, const CUtensorMap& mapW,
                                      const CUtensorMap* mapsC, const GroupTable& g,
                                      const GemmShape& s, int64_t bias_group_stride, int grid,
                                      size_t smem, cudaStream_t stream);

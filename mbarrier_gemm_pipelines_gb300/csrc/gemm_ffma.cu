@@ -5,16 +5,24 @@
 // ring buffer of section 3.4: a producer role moves K tiles into a stage ring
 // while consumer roles compute on full stages and hand them back.
 //
-// Roles (one CTA = 3 warpgroups, 384 threads, "gpu_warp_specialization",
-// "The architecture: every piece explained": whole warps take whole jobs,
-// and the register budget moves from the producers to the consumers):
+// Roles ("gpu_warp_specialization", "The architecture: every piece
+// explained": whole warps take whole jobs, and the register budget moves from
+// the producers to the consumers):
 //   warpgroup 0  warp 0 lane 0 = TMA producer; the group gives up registers
-//   warpgroups 1-2 (8 warps)   = FFMA consumers, one 8x8 register micro-tile
-//                                 per thread of a 128x128 output tile
+//   CW consumer warps           = FFMA consumers of a 128x128 output tile:
+//     CW = 8 (default): 2 warpgroups, 384 threads per CTA, an 8x8 register
+//                       micro-tile per thread, 2 consumer warps per scheduler
+//     CW = 16:          4 warpgroups, 640 threads per CTA, an 8x4 micro-tile,
+//                       4 consumer warps per scheduler
+// A thread reads rows + columns floats from shared memory per k for
+// rows x columns FMAs: 16 per 64 at 8x8, 12 per 32 at 8x4.  Measured on GB300
+// the 8x4 layout keeps the FMA pipe busy 63% of active cycles against 74.5%
+// at 8x8 (48.8 against 57 TFLOP/s): more warps per scheduler do not pay for
+// the extra shared-memory traffic per FMA.
 // Ring: S stages of { A 128x32 fp32, 128-byte swizzled rows;
 //                     B 32x128 fp32 as four 32-column 128-byte swizzled panels }.
 // full[s]: 1 arrival (producer's arrive.expect_tx) + 32 KiB of TMA bytes.
-// empty[s]: 8 arrivals, one per consumer warp after its last read of the slot.
+// empty[s]: CW arrivals, one per consumer warp after its last read of the slot.
 // Slot/parity of k-iteration i (running across this CTA's tiles):
 //   slot = i % S, full parity = (i / S) & 1, empty parity = ((i / S) & 1) ^ 1.
 #include "gbr_internal.h"
@@ -23,12 +31,26 @@ namespace gbr {
 
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int kConsumerWarps = 8;
 constexpr uint32_t kABytes = kFfmaBM * kFfmaBK * 4;   // 16 KiB
 constexpr uint32_t kBPanelBytes = kFfmaBK * 128;      // 32 rows x 128 B
-constexpr uint32_t kProducerRegs = 40;
-constexpr uint32_t kConsumerRegs = 232;
+
+// Consumer layouts of the 128 x 128 tile.  np: packed column pairs per thread
+// (8 rows x 2 np columns).  The register split (producer warpgroup + consumers)
+// must fit in what the CTA is launched with: threads x launch registers.
+template <int CW>
+struct Cons;
+template <>
+struct Cons<8> {
+    static constexpr int threads = 256, np = 4;
+    static constexpr uint32_t regs = 232, producer_regs = 40;
+};
+template <>
+struct Cons<16> {
+    static constexpr int threads = 512, np = 2;
+    static constexpr uint32_t regs = 104, producer_regs = 64;
+};
+template <int CW>
+constexpr int kThreads = 128 + Cons<CW>::threads;
 
 // One 32-deep K stage of the 128 x 128 tile for thread (tx, ty): rows
 // ty + 16 r, columns 4 tx .. 4 tx + 3 and 64 + 4 tx .. 64 + 4 tx + 3.  All of
@@ -41,7 +63,10 @@ constexpr uint32_t kConsumerRegs = 232;
 // (two IEEE fp32 FMAs, the same results as two scalar ones) of A broadcast to
 // both halves and a B pair read straight from shared memory as 64 bits.  Half
 // as many FMA instructions leave issue slots for the loads.
-__device__ __forceinline__ void ffma_stage(uint64_t (&acc)[8][4], const uint8_t* As,
+//
+// NP = 2 (the 16-warp layout): columns 4 tx .. 4 tx + 3 only, one B pair load.
+template <int NP>
+__device__ __forceinline__ void ffma_stage(uint64_t (&acc)[8][NP], const uint8_t* As,
                                            const uint8_t* Bs, uint32_t a_row, uint32_t a_ph,
                                            const uint32_t (&b_sw)[8]) {
 #pragma unroll
@@ -55,27 +80,34 @@ __device__ __forceinline__ void ffma_stage(uint64_t (&acc)[8][4], const uint8_t*
             const uint32_t k = 4 * k4 + kk;
             const uint8_t* bp = Bs + b_sw[k & 7u] + k * 128u;
             const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(bp);
-            const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(bp + 2 * kBPanelBytes);
+            uint64_t bj[NP];
+            bj[0] = b0.x;
+            bj[1] = b0.y;
+            if (NP == 4) {
+                const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(bp + 2 * kBPanelBytes);
+                bj[NP > 2 ? 2 : 0] = b1.x;
+                bj[NP > 2 ? 3 : 1] = b1.y;
+            }
             uint64_t a2[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r)
                 a2[r] = ptx::f32x2_splat(kk == 0 ? a[r].x : kk == 1 ? a[r].y : kk == 2 ? a[r].z : a[r].w);
-            const uint64_t bj[4] = {b0.x, b0.y, b1.x, b1.y};
             // Column pair outer, row inner: eight independent FMAs share one B
             // pair (measured 4% faster than the row-outer order).
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < NP; ++j)
 #pragma unroll
                 for (int r = 0; r < 8; ++r) ptx::fma_f32x2(acc[r][j], a2[r], bj[j]);
         }
     }
 }
 
-__device__ __forceinline__ void ffma_zero(uint64_t (&acc)[8][4]) {
+template <int NP>
+__device__ __forceinline__ void ffma_zero(uint64_t (&acc)[8][NP]) {
 #pragma unroll
     for (int r = 0; r < 8; ++r)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[r][j] = 0ull;
+        for (int j = 0; j < NP; ++j) acc[r][j] = 0ull;
 }
 
 __device__ __forceinline__ void ffma_tables(uint32_t tx, uint32_t ty, uint32_t& a_row,
@@ -87,13 +119,31 @@ __device__ __forceinline__ void ffma_tables(uint32_t tx, uint32_t ty, uint32_t& 
         b_sw[j] = (tx >> 3) * kBPanelBytes + (((tx & 7u) ^ j) << 4);  // column 4 tx, K row % 8 = j
 }
 
-// C = max(0, acc + bias) for the thread's 8 x 8 outputs of tile (mt, nt).
-__device__ __forceinline__ void ffma_epilogue(const uint64_t (&acc)[8][4], const GemmShape& p,
+// Thread (tx, ty) of consumer `ct` in the CW-warp layout.  CW = 8: 16 x 16
+// threads, tx fastest.  CW = 16: 32 x 16 threads, each warp 8 tx x 4 ty, so
+// that one warp's A reads touch 4 rows (distinct swizzle phases) and its B
+// reads 8 chunks of one 128-byte panel row: one wavefront each.
+template <int CW>
+__device__ __forceinline__ void ffma_thread(uint32_t ct, uint32_t& tx, uint32_t& ty) {
+    if (CW == 8) {
+        tx = ct & 15u;
+        ty = ct >> 4;
+    } else {
+        const uint32_t w = ct >> 5, l = ct & 31u;
+        tx = 8u * (w >> 2) + (l & 7u);
+        ty = 4u * (w & 3u) + (l >> 3);
+    }
+}
+
+// C = max(0, acc + bias) for the thread's 8 x (2 NP) outputs of tile (mt, nt):
+// rows ty + 16 r, columns 4 tx + 64 h + (0..3).
+template <int NP>
+__device__ __forceinline__ void ffma_epilogue(const uint64_t (&acc)[8][NP], const GemmShape& p,
                                               uint32_t mt, uint32_t nt, uint32_t tx, uint32_t ty) {
     float* C = static_cast<float*>(p.C);
     const int n0 = int(nt) * kFfmaBN, m0 = int(mt) * kFfmaBM;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NP / 2; ++h) {
         const int n = n0 + int(4 * tx) + 64 * h;
         if (n >= p.N) continue;
         const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + n));
@@ -118,10 +168,11 @@ __device__ __forceinline__ void ffma_epilogue(const uint64_t (&acc)[8][4], const
 // warpgroup copies the stage with 16-byte cp.async per thread into the same
 // swizzled layout, and each of its 128 threads arrives on full[s] with
 // cp.async.mbarrier.arrive.noinc once its own copies have landed.
-template <bool CPASYNC>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int CW, bool CPASYNC>
+__global__ void __launch_bounds__(kThreads<CW>, 1)
     gemm_ffma_kernel(const __grid_constant__ CUtensorMap mapA,
                      const __grid_constant__ CUtensorMap mapB, const GemmShape p) {
+    using L = Cons<CW>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = align_1024(smem_raw);
     const int S = p.stages;
@@ -133,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(ptx::smem_addr(full + s), CPASYNC ? 128u : 1u);
-            ptx::mbar_init(ptx::smem_addr(empty + s), kConsumerWarps);
+            ptx::mbar_init(ptx::smem_addr(empty + s), CW);
         }
         *abort_flag = 0;
         ptx::fence_barrier_init();
@@ -150,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t issued = 0;   // TMA producer lane: ring items registered on full[]
 
     if (warp < 4) {
-        ptx::setmaxnreg_dec<kProducerRegs>();
+        ptx::setmaxnreg_dec<L::producer_regs>();
         if (CPASYNC) {
             // ------------------------------------ cp.async producer warpgroup
             const uint32_t pt = threadIdx.x;   // 0..127
@@ -230,17 +281,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             issued = i;
         }
     } else {
-        ptx::setmaxnreg_inc<kConsumerRegs>();
+        ptx::setmaxnreg_inc<L::regs>();
         // ---------------------------------------------------- consumers
-        // Thread (tx, ty) of 16 x 16 owns rows ty + 16 r (r = 0..7) and columns
-        // 4 tx .. 4 tx + 3 and 64 + 4 tx .. 64 + 4 tx + 3 of the 128 x 128 tile.
-        // All its rows have the same (row % 8), so every A read of a k-group
-        // uses one swizzle phase; all its columns sit at the same position
-        // inside their 32-column panels, so every B read of a k uses one
-        // phase too.  The phases come from two 8-entry tables and every
-        // shared-memory load is base + immediate offset.
-        const uint32_t ct = threadIdx.x - 128;        // 0..255
-        const uint32_t tx = ct & 15u, ty = ct >> 4;
+        // Thread (tx, ty) owns rows ty + 16 r (r = 0..7) and columns
+        // 4 tx .. 4 tx + 3 (and, at CW = 8, 64 + 4 tx .. 64 + 4 tx + 3) of the
+        // 128 x 128 tile.  All its rows have the same (row % 8), so every A
+        // read of a k-group uses one swizzle phase; all its columns sit at the
+        // same position inside their 32-column panels, so every B read of a k
+        // uses one phase too.  The phases come from two 8-entry tables and
+        // every shared-memory load is base + immediate offset.
+        const uint32_t ct = threadIdx.x - 128;
+        uint32_t tx, ty;
+        ffma_thread<CW>(ct, tx, ty);
         uint32_t a_row, a_ph, b_sw[8];
         ffma_tables(tx, ty, a_row, a_ph, b_sw);
 
@@ -250,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
             uint32_t mt, nt;
             raster_tile(t, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
-            uint64_t acc[8][4];
+            uint64_t acc[8][L::np];
             ffma_zero(acc);
 
             for (int kb = 0; kb < p.num_kb; ++kb, ++i) {
@@ -294,31 +346,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 // block synchronises again before the buffer may be overwritten.  Same tile,
 // same shared-memory layout and same FFMA micro-kernel as the warp-specialized
 // kernel above; no roles, no ring, no mbarriers.  One CTA per output tile.
-constexpr int kSyncThreads = 256;
-
-__global__ void __launch_bounds__(kSyncThreads, 2) gemm_ffma_sync_kernel(const float* __restrict__ A,
-                                                                         const float* __restrict__ B,
-                                                                         const GemmShape p) {
+// Threads per CTA: the CW consumer layout's (256: 2 CTAs per SM, 512: 1).
+template <int CW>
+__global__ void __launch_bounds__(Cons<CW>::threads, CW == 8 ? 2 : 1)
+    gemm_ffma_sync_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                          const GemmShape p) {
+    constexpr int kSyncThreads = Cons<CW>::threads;
+    constexpr int kLoads = 1024 / kSyncThreads;   // 16-byte chunks of A (and of B) per thread
     __shared__ __align__(1024) uint8_t tile[kFfmaStageBytes];
     uint8_t* As = tile;
     uint8_t* Bs = tile + kABytes;
     const uint32_t t = threadIdx.x;
-    const uint32_t tx = t & 15u, ty = t >> 4;
+    uint32_t tx, ty;
+    ffma_thread<CW>(t, tx, ty);
     uint32_t mt, nt;
     raster_tile(blockIdx.x, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
     const int m0 = int(mt) * kFfmaBM, n0 = int(nt) * kFfmaBN;
     uint32_t a_row, a_ph, b_sw[8];
     ffma_tables(tx, ty, a_row, a_ph, b_sw);
-    uint64_t acc[8][4];
+    uint64_t acc[8][Cons<CW>::np];
     ffma_zero(acc);
 
     for (int kb = 0; kb < p.num_kb; ++kb) {
         const int k0 = kb * kFfmaBK;
-        // load: 4 float4 of A (row idx/8, 16-byte chunk idx%8) and 4 of B
+        // load: kLoads float4 of A (row idx/8, 16-byte chunk idx%8) and of B
         // (K row idx/32, 16-byte chunk idx%32) per thread, zero outside the
         // matrix, stored in the same swizzled layout the TMA path produces.
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kLoads; ++j) {
             const uint32_t idx = t + kSyncThreads * j;
             const uint32_t row = idx >> 3, k4 = idx & 7u;
             const int m = m0 + int(row), k = k0 + int(4 * k4);
@@ -327,7 +382,7 @@ __global__ void __launch_bounds__(kSyncThreads, 2) gemm_ffma_sync_kernel(const f
             *reinterpret_cast<float4*>(As + row * 128u + ((k4 ^ (row & 7u)) << 4)) = v;
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kLoads; ++j) {
             const uint32_t idx = t + kSyncThreads * j;
             const uint32_t kr = idx >> 5, n4 = idx & 31u;
             const int k = k0 + int(kr), n = n0 + int(4 * n4);
@@ -343,11 +398,37 @@ __global__ void __launch_bounds__(kSyncThreads, 2) gemm_ffma_sync_kernel(const f
     ffma_epilogue(acc, p, mt, nt, tx, ty);
 }
 
+int g_ffma_warps = 8;    // consumer warps of the FFMA kernels (8 or 16)
+std::mutex g_ffma_mu;
+
+int ffma_warps_now() {
+    std::lock_guard<std::mutex> lk(g_ffma_mu);
+    return g_ffma_warps;
+}
+
+template <int CW>
+const void* ffma_fn(bool cpasync) {
+    return cpasync ? reinterpret_cast<const void*>(gemm_ffma_kernel<CW, true>)
+                   : reinterpret_cast<const void*>(gemm_ffma_kernel<CW, false>);
+}
+
 }  // namespace
+
+int ffma_consumer_warps() { return ffma_warps_now(); }
+
+int ffma_set_consumer_warps(int cw) {
+    if (cw != 8 && cw != 16) return -1;
+    std::lock_guard<std::mutex> lk(g_ffma_mu);
+    g_ffma_warps = cw;
+    return 0;
+}
 
 cudaError_t launch_gemm_ffma_sync(const float* A, const float* B, const GemmShape& s,
                                   cudaStream_t stream) {
-    gemm_ffma_sync_kernel<<<s.num_tiles, kSyncThreads, 0, stream>>>(A, B, s);
+    if (ffma_warps_now() == 16)
+        gemm_ffma_sync_kernel<16><<<s.num_tiles, Cons<16>::threads, 0, stream>>>(A, B, s);
+    else
+        gemm_ffma_sync_kernel<8><<<s.num_tiles, Cons<8>::threads, 0, stream>>>(A, B, s);
     return cudaGetLastError();
 }
 
@@ -357,50 +438,65 @@ size_t ffma_smem_bytes(int stages) {
 
 cudaError_t ffma_prepare(size_t smem) {
     static std::mutex mu;
-    static size_t set[kMaxDeviceSlots][2] = {};
+    static size_t set[kMaxDeviceSlots][4] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDeviceSlots) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(mu);
-    if ((e = raise_smem_limit(reinterpret_cast<const void*>(gemm_ffma_kernel<false>), smem,
-                              &set[dev][0])) != cudaSuccess)
-        return e;
-    return raise_smem_limit(reinterpret_cast<const void*>(gemm_ffma_kernel<true>), smem, &set[dev][1]);
+    const void* fns[4] = {ffma_fn<8>(false), ffma_fn<8>(true), ffma_fn<16>(false),
+                          ffma_fn<16>(true)};
+    for (int i = 0; i < 4; ++i)
+        if ((e = raise_smem_limit(fns[i], smem, &set[dev][i])) != cudaSuccess) return e;
+    return cudaSuccess;
 }
 
 cudaError_t ffma_occupancy(size_t smem, int* blocks_per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, gemm_ffma_kernel<false>,
-                                                         kThreads, smem);
+    if (ffma_warps_now() == 16)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            blocks_per_sm, gemm_ffma_kernel<16, false>, kThreads<16>, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, gemm_ffma_kernel<8, false>,
+                                                         kThreads<8>, smem);
 }
 
 // The register split must fit in what the CTA is launched with, or the
 // consumers' setmaxnreg.inc would wait forever for registers.
-cudaError_t ffma_check_registers(int* regs) {
-    const long need = 128L * kProducerRegs + 256L * kConsumerRegs;
-    for (const void* fn : {reinterpret_cast<const void*>(gemm_ffma_kernel<false>),
-                           reinterpret_cast<const void*>(gemm_ffma_kernel<true>)}) {
+template <int CW>
+cudaError_t ffma_check_registers_cw(int* regs) {
+    const long need = 128L * Cons<CW>::producer_regs + long(Cons<CW>::threads) * Cons<CW>::regs;
+    for (const void* fn : {ffma_fn<CW>(false), ffma_fn<CW>(true)}) {
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, fn);
         if (e != cudaSuccess) return e;
         *regs = fa.numRegs;
-        if (long(fa.numRegs) * kThreads < need) return cudaErrorInvalidConfiguration;
+        if (long(fa.numRegs) * kThreads<CW> < need) return cudaErrorInvalidConfiguration;
     }
     return cudaSuccess;
 }
 
+cudaError_t ffma_check_registers(int* regs) {
+    cudaError_t e = ffma_check_registers_cw<8>(regs);
+    if (e != cudaSuccess) return e;
+    return ffma_check_registers_cw<16>(regs);
+}
+
 cudaError_t launch_gemm_ffma(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmShape& s,
                              int grid, size_t smem, cudaStream_t stream, bool cpasync) {
+    const int cw = ffma_warps_now();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(cw == 16 ? kThreads<16> : kThreads<8>);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     cfg.numAttrs = programmatic_launch_attr(attr);
     cfg.attrs = attr;
-    if (cpasync) return cudaLaunchKernelEx(&cfg, gemm_ffma_kernel<true>, mapA, mapB, s);
-    return cudaLaunchKernelEx(&cfg, gemm_ffma_kernel<false>, mapA, mapB, s);
+    if (cw == 16) {
+        if (cpasync) return cudaLaunchKernelEx(&cfg, gemm_ffma_kernel<16, true>, mapA, mapB, s);
+        return cudaLaunchKernelEx(&cfg, gemm_ffma_kernel<16, false>, mapA, mapB, s);
+    }
+    if (cpasync) return cudaLaunchKernelEx(&cfg, gemm_ffma_kernel<8, true>, mapA, mapB, s);
+    return cudaLaunchKernelEx(&cfg, gemm_ffma_kernel<8, false>, mapA, mapB, s);
 }
 
 }  // namespace gbr

@@ -56,7 +56,7 @@ cudaError_t launch_umma(int kind, int pair, const UmmaParams<GROUPED>& P, int gr
 
 size_t umma_ring_bytes(int stages, int pair, int k_sub) {
     const size_t stage = pair == 2 ? Pair<2>::stage_bytes : Pair<1>::stage_bytes;
-    return 1024 + size_t(stages) * size_t(k_sub) * stage + kUmmaEpiBytes + 256;
+    return 1024 + size_t(stages) * size_t(k_sub) * stage + kUmmaEpiBytes + kUmmaBarrierBytes;
 }
 
 size_t umma_smem_bytes(int stages, int pair, int k_sub) {
@@ -126,13 +126,15 @@ cudaError_t launch_gemm_umma(int kind, const CUtensorMap& mapA, const CUtensorMa
     return launch_gemm_umma(kind, 1, mapA, mapB, mapC, s, grid, smem, stream);
 }
 
-cudaError_t launch_gemm_umma_grouped(int pair, const CUtensorMap& mapX, const CUtensorMap& mapW,
+cudaError_t launch_gemm_umma_grouped(int pair, const CUtensorMap& mapX,
+                                     const CUtensorMap& mapX_thin, const CUtensorMap& mapW,
                                      const CUtensorMap* mapsC, const GroupTable& g,
                                      const GemmShape& s, int64_t bias_group_stride, int grid,
                                      size_t smem, cudaStream_t stream) {
     UmmaParams<true> P;
     memset(&P, 0, sizeof(P));
     P.mapA = mapX;
+    P.mapA_thin = mapX_thin;
     P.mapB = mapW;
     for (int e = 0; e < g.num_groups; ++e) P.mapC[e] = mapsC[e];
     P.s = s;

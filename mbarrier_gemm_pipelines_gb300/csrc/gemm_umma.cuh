@@ -157,6 +157,7 @@ __device__ __forceinline__ void load_box_3d(uint32_t dst, const CUtensorMap* map
 template <bool GROUPED>
 struct UmmaParams {
     CUtensorMap mapA;
+    CUtensorMap mapA_thin;   // grouped: X in boxes of kThinBoxRows rows (thin tiles)
     CUtensorMap mapB;
     CUtensorMap mapC[GROUPED ? kMaxGroups : 1];
     GemmShape s;
@@ -166,18 +167,47 @@ struct UmmaParams {
 
 struct TileInfo {
     int32_t a_row;   // row coordinate of this CTA's A/X box
-    int32_t c_row;   // row coordinate of this CTA's C rows in mapC[group]
+    int32_t c_row;   // row coordinate of this CTA's C rows in mapC[group] (thin: the tile's)
     int32_t n0;      // first output column of the tile
     int32_t group;
+    int32_t thin;    // 0, or the rows of a transposed (thin) tile (its MMA N: rounded up to 16)
 };
+
+// A thin tile's X rows are loaded in boxes of this many rows (2 KiB of bf16
+// per 128-byte K slice), only as many as the tile uses.
+constexpr uint32_t kThinBoxRows = 16;
+
+// Bytes one CTA loads per ring stage of a tile: a thin tile's t rows need
+// n_pad / 2 rows of X per CTA, in ceil(n_pad / 2 / kThinBoxRows) boxes.
+template <int PAIR>
+__device__ __forceinline__ uint32_t cta_stage_bytes(int32_t thin, uint32_t ksub) {
+    if (thin <= 0) return ksub * Pair<PAIR>::stage_bytes;
+    const uint32_t rows = uint32_t((thin + 15) & ~15) / 2u;
+    const uint32_t boxes = (rows + kThinBoxRows - 1) / kThinBoxRows;
+    return ksub * (boxes * kThinBoxRows * 128u + Pair<PAIR>::b_bytes);
+}
+
+// Instruction descriptor of a thin tile (CTA pair, bf16): the MMA computes
+// C^T = W^T X^T, with A = W^T (the tile's 256 weight columns, MN-major: the
+// same N-major panels the ordinary tile reads as B) and B = X^T (the tile's
+// rows, K-major: the same boxes the ordinary tile reads as A); M = 256,
+// N = n_pad.
+__device__ __forceinline__ uint32_t make_idesc_thin(uint32_t n_pad) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (0u << 16) | ((n_pad >> 3) << 17) |
+           ((256u >> 4) << 24);
+}
 
 template <bool GROUPED, int PAIR>
 __device__ __forceinline__ TileInfo decode_tile(const UmmaParams<GROUPED>& P, uint32_t t,
                                                 uint32_t rank) {
     TileInfo ti;
+    ti.thin = 0;
     uint32_t mt, nt;
     if (!GROUPED) {
-        raster_tile(t, P.s.m_tiles, P.s.n_tiles, P.s.group_m, mt, nt);
+        if (P.s.group_n > 0)
+            raster_tile_cols(t, P.s.m_tiles, P.s.n_tiles, P.s.group_n, mt, nt);
+        else
+            raster_tile(t, P.s.m_tiles, P.s.n_tiles, P.s.group_m, mt, nt);
         ti.c_row = int32_t(mt * Pair<PAIR>::tile_m + rank * 128);
         ti.a_row = ti.c_row;
         ti.group = 0;
@@ -189,6 +219,13 @@ __device__ __forceinline__ TileInfo decode_tile(const UmmaParams<GROUPED>& P, ui
         ti.c_row = int32_t(mt * Pair<PAIR>::tile_m + rank * 128);
         ti.a_row = P.g.row_off[e] + ti.c_row;
         ti.group = e;
+        if (PAIR == 2 && P.g.thin[e] > 0 && int32_t(mt) + 1 == P.g.m_tiles[e]) {
+            // Thin tile: the tile's rows are the MMA's N columns, half of them
+            // (n_pad / 2 rows of X) from each CTA of the pair.
+            ti.thin = P.g.thin[e];
+            ti.c_row = int32_t(mt * Pair<PAIR>::tile_m);
+            ti.a_row = P.g.row_off[e] + ti.c_row + int32_t(rank) * (((ti.thin + 15) & ~15) / 2);
+        }
     }
     ti.n0 = int32_t(nt) * kUmmaBN;
     return ti;
@@ -318,6 +355,77 @@ __device__ __forceinline__ void acc_release(uint32_t ae, uint32_t lane) {
     }
 }
 
+// Epilogue of a thin tile (grouped, CTA pair): C^T sits in TMEM, lane =
+// output column `col` of the tile (n0 + col), column j = row j of the tile.
+// Each lane writes its column of the tile's rows with bias and ReLU; for a
+// given row the warp's lanes write 32 consecutive columns.  The accumulator
+// may be released once this returns (every tcgen05.ld has completed).
+__device__ __forceinline__ void thin_epilogue(const GemmShape& s, const TileInfo& ti,
+                                              const float* bias, int32_t group_row0,
+                                              uint32_t tcol, uint32_t col, bool zero_acc) {
+    const int n = ti.n0 + int(col);
+    const bool col_in = n < s.N;
+    const float bv = col_in ? __ldg(bias + n) : 0.f;
+    const size_t pitch = size_t(s.N);
+    __nv_bfloat16* cp = static_cast<__nv_bfloat16*>(s.C) +
+                        size_t(group_row0 + ti.c_row) * pitch + size_t(n);
+    const int n_pad = (ti.thin + 15) & ~15;
+#pragma unroll 1
+    for (int c = 0; c < n_pad; c += 16) {
+        uint32_t r[16];
+        ptx::tmem_ld_32x32b_x16(tcol + uint32_t(c), r);
+        ptx::tmem_ld_wait();
+        const int rows = col_in ? ti.thin - c : 0;   // rows of this chunk to store
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j < rows)
+                *cp = __float2bfloat16_rn(fmaxf((zero_acc ? 0.f : __uint_as_float(r[j])) + bv, 0.f));
+            cp += pitch;
+        }
+    }
+}
+
+// The MMAs of one ring stage (KSUB 128-byte K slices) into accumulator d_tmem.
+// THIN (grouped, CTA pair, bf16): the tile is computed transposed, so the
+// weight panels are the A operand and the X rows the B operand, with the thin
+// instruction descriptor.  `first`: this stage starts the accumulation.
+template <int KIND, int PAIR, uint32_t KSUB, bool THIN>
+__device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint32_t stage_base, bool first,
+                                            uint32_t thin_idesc) {
+    using K_ = Kind<KIND>;
+    using PR = Pair<PAIR>;
+    constexpr uint32_t kPanelBytes = K_::bk * 128;
+    constexpr uint32_t kIdesc = make_idesc<KIND, PAIR>();
+#pragma unroll
+    for (uint32_t h = 0; h < KSUB; ++h) {
+        const uint32_t a_base = stage_base + h * kUmmaAStageBytes;
+        const uint32_t b_base = stage_base + KSUB * kUmmaAStageBytes + h * PR::b_bytes;
+#pragma unroll
+        for (uint32_t k = 0; k < 128 / (K_::mma_k * K_::esize); ++k) {
+            const uint64_t ad = sw128_desc(a_base + k * K_::mma_k * K_::esize, 16, 1024);
+            const uint64_t bd = K_::b_kmajor
+                                    ? sw128_desc(b_base + k * K_::mma_k * K_::esize, 16, 1024)
+                                    : sw128_desc(b_base + k * K_::mma_k * 128, kPanelBytes, 1024);
+            const uint32_t acc = (!first || h != 0 || k != 0) ? 1u : 0u;
+            if (PAIR == 2) {
+                if (KIND == kUmmaBf16) {
+                    if (THIN)
+                        ptx::mma_f16_pair(d_tmem, bd, ad, thin_idesc, acc);
+                    else
+                        ptx::mma_f16_pair(d_tmem, ad, bd, kIdesc, acc);
+                } else {
+                    ptx::mma_tf32_pair(d_tmem, ad, bd, kIdesc, acc);
+                }
+            } else {
+                if (KIND == kUmmaBf16)
+                    ptx::mma_f16(d_tmem, ad, bd, kIdesc, acc);
+                else
+                    ptx::mma_tf32(d_tmem, ad, bd, kIdesc, acc);
+            }
+        }
+    }
+}
+
 // Teardown after an abort, by the even CTA's producer lane once every role of
 // the unit has left its loop: waits (bounded) until every TMA load that this
 // CTA or its peer issued has landed, so that no copy still writes shared
@@ -330,9 +438,11 @@ __device__ __forceinline__ void acc_release(uint32_t ae, uint32_t lane) {
 // Registrations are evened up first: the peer's half of an item it never
 // issued is counted done (complete_tx), and an item only the peer issued gets
 // the arrival and expect_tx of the peer's half.
+// Each producer records in slot_bytes[slot] the bytes its own copies of the
+// slot's latest item move (both CTAs of a pair move the same for an item).
 template <int PAIR>
 __device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t S, uint32_t issued,
-                                           uint32_t issued_peer, uint32_t cta_bytes,
+                                           uint32_t issued_peer, const uint32_t* slot_bytes,
                                            const FaultInjection& inj, uint32_t unit,
                                            uint64_t limit_ns) {
     const uint32_t hi = issued > issued_peer ? issued : issued_peer;
@@ -343,8 +453,12 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t S, uint32_t 
         const bool mine = j < issued, peer = PAIR == 2 && j < issued_peer;
         if (PAIR == 2) {
             if (!mine && !peer) continue;
-            if (mine && !peer) ptx::mbar_complete_tx(bar, cta_bytes);
-            if (!mine && peer) ptx::mbar_arrive_expect_tx(bar, cta_bytes);
+            if (mine && !peer) ptx::mbar_complete_tx(bar, slot_bytes[j % S]);
+            if (!mine && peer) {
+                const uint32_t peer_bytes = ptx::ld_shared_cluster_u32(
+                    ptx::mapa_shared(ptx::smem_addr(slot_bytes + j % S), 1));
+                ptx::mbar_arrive_expect_tx(bar, peer_bytes);
+            }
         } else if (!mine) {
             continue;
         }
@@ -386,6 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tiles.empty = tiles.full + kTileRing;
     tiles.ids = reinterpret_cast<uint32_t*>(tiles.empty + kTileRing);
     uint32_t* issued_word = tiles.ids + kTileRing;   // ring items this CTA's producer issued
+    uint32_t* slot_bytes = issued_word + 1;          // [S]: bytes of this CTA's copies per slot
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const uint32_t rank = PAIR == 2 ? ptx::cluster_ctarank() : 0u;
@@ -458,6 +573,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                  ++j) {
                 const TileInfo ti = decode_tile<GROUPED, PAIR>(P, w.tile, rank);
                 const int32_t bcol0 = ti.n0 + int32_t(rank * PR::b_cols);
+                const bool thin = GROUPED && PAIR == 2 && ti.thin > 0;
+                const uint32_t my_bytes = cta_stage_bytes<PAIR>(thin ? ti.thin : 0, ksub);
+                const uint32_t thin_boxes =
+                    thin ? (uint32_t((ti.thin + 15) & ~15) / 2u + kThinBoxRows - 1) / kThinBoxRows : 0u;
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const uint32_t slot = it % S, ph = (it / S) & 1u;
                     if (!mbar_wait<kCl>(ptx::smem_addr(empty + slot), ph ^ 1u, s.ctl, abort_flag,
@@ -468,7 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (kTrace) trace_event(s.ctl, kRoleProducer, ntr, kEvWaitDone, it, slot, ph ^ 1u);
                     const uint32_t fb_local = ptx::smem_addr(full + slot);
                     const uint32_t fb = PAIR == 2 ? ptx::mapa_shared(fb_local, 0) : fb_local;
-                    if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, PAIR * stage_bytes);
+                    slot_bytes[slot] = my_bytes;
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, PAIR * my_bytes);
                     if (inject_skip_unit(s.inject, unit, it)) continue;   // self test
                     if (kTrace) trace_event(s.ctl, kRoleProducer, ntr, kEvIssued, it, slot, 0);
                     const uint32_t stage_base = ring_base + slot * stage_bytes;
@@ -478,7 +598,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t b_dst =
                             stage_base + ksub * kUmmaAStageBytes + h * PR::b_bytes;
                         const int32_t k0 = (kb * int32_t(ksub) + int32_t(h)) * int32_t(K_::bk);
-                        load_box_2d<PAIR>(a_dst, &P.mapA, fb, k0, ti.a_row, hint, pol_a);
+                        if (GROUPED && PAIR == 2 && thin) {
+                            for (uint32_t i = 0; i < thin_boxes; ++i)
+                                load_box_2d<PAIR>(a_dst + i * kThinBoxRows * 128u, &P.mapA_thin, fb,
+                                                  k0, ti.a_row + int32_t(i * kThinBoxRows), hint,
+                                                  pol_a);
+                        } else {
+                            load_box_2d<PAIR>(a_dst, &P.mapA, fb, k0, ti.a_row, hint, pol_a);
+                        }
                         if (K_::b_kmajor) {
                             // Bt[N, K]: one box of this CTA's b_cols rows, 128 bytes of K each.
                             load_box_2d<PAIR>(b_dst, &P.mapB, fb, k0, bcol0, hint, pol_b);
@@ -517,6 +644,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kTrace) trace_event(s.ctl, kRoleMmaAcc, nta, kEvWaitDone, tl, a, aph ^ 1u);
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + a * kAccCols;
+                // Thin tile (grouped, CTA pair): A and B swap roles (C^T = W^T X^T).
+                uint32_t thin_idesc = 0;
+                if (GROUPED && PAIR == 2) {
+                    const TileInfo ti = decode_tile<GROUPED, PAIR>(P, w.tile, 0);
+                    if (ti.thin > 0) thin_idesc = make_idesc_thin(uint32_t(ti.thin + 15) & ~15u);
+                }
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const uint32_t slot = it % S, ph = (it / S) & 1u;
                     if (!mbar_wait<kCl>(ptx::smem_addr(full + slot), ph, s.ctl, abort_flag,
@@ -527,31 +660,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (kTrace) trace_event(s.ctl, kRoleConsumer, ntr, kEvWaitDone, it, slot, ph);
                     ptx::tc_fence_after_sync();
                     const uint32_t stage_base = ring_base + slot * stage_bytes;
-#pragma unroll
-                    for (uint32_t h = 0; h < ksub; ++h) {
-                    const uint32_t a_base = stage_base + h * kUmmaAStageBytes;
-                    const uint32_t b_base = stage_base + ksub * kUmmaAStageBytes + h * PR::b_bytes;
-#pragma unroll
-                    for (uint32_t k = 0; k < 128 / (K_::mma_k * K_::esize); ++k) {
-                        const uint64_t ad = sw128_desc(a_base + k * K_::mma_k * K_::esize, 16, 1024);
-                        const uint64_t bd =
-                            K_::b_kmajor
-                                ? sw128_desc(b_base + k * K_::mma_k * K_::esize, 16, 1024)
-                                : sw128_desc(b_base + k * K_::mma_k * 128, kPanelBytes, 1024);
-                        const uint32_t acc = (uint32_t(kb - w.kb0) | h | k) != 0;
-                        if (PAIR == 2) {
-                            if (KIND == kUmmaBf16)
-                                ptx::mma_f16_pair(d_tmem, ad, bd, kIdesc, acc);
-                            else
-                                ptx::mma_tf32_pair(d_tmem, ad, bd, kIdesc, acc);
-                        } else {
-                            if (KIND == kUmmaBf16)
-                                ptx::mma_f16(d_tmem, ad, bd, kIdesc, acc);
-                            else
-                                ptx::mma_tf32(d_tmem, ad, bd, kIdesc, acc);
-                        }
-                    }
-                    }
+                    if (GROUPED && PAIR == 2 && KIND == kUmmaBf16 && thin_idesc != 0)
+                        issue_stage<KIND, PAIR, KSUB, true>(d_tmem, stage_base, kb == w.kb0,
+                                                            thin_idesc);
+                    else
+                        issue_stage<KIND, PAIR, KSUB, false>(d_tmem, stage_base, kb == w.kb0, 0u);
                     if (kTrace) trace_event(s.ctl, kRoleConsumer, ntr, kEvReleased, it, slot, 0);
                     if (PAIR == 2)
                         ptx::mma_commit_pair_multicast(ptx::smem_addr(empty + slot), 0x3);
@@ -650,6 +763,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sum = blk;
             }
             const float* bias = s.bias + (GROUPED ? P.bias_group_stride * ti.group : 0);
+            if (GROUPED && PAIR == 2 && KIND == kUmmaBf16 && ti.thin > 0) {
+                // Thin tile: the accumulator holds C^T, TMEM lane = output
+                // column, column j = row j of the tile.  Each lane stores its
+                // column of the tile's rows; a warp's 32 lanes write 64
+                // contiguous bytes of a row.  (Thin tiles are never split.)
+                thin_epilogue(s, ti, bias, P.g.row_off[ti.group], tmem_base + lane_base + a * kAccCols,
+                              rank * 128u + q * 32u + lane, zero_acc);
+                if (tracer) trace_event(s.ctl, kRoleEpilogue, ntr, kEvReleased, tl, a, 0);
+                acc_release<PAIR>(ae, lane);
+                continue;
+            }
             const CUtensorMap* mapC = &P.mapC[GROUPED ? ti.group : 0];
             for (uint32_t c = 0; c < kChunks; ++c, ++chunk_ctr) {
                 const uint32_t col0 = c * K_::out_chunk_cols;
@@ -751,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issued_peer = ptx::ld_shared_cluster_u32(ptx::mapa_shared(ptx::smem_addr(issued_word), 1));
         }
         if (aborted)
-            drain_ring<PAIR>(full, uint32_t(S), issued, issued_peer, stage_bytes, s.inject, unit,
+            drain_ring<PAIR>(full, uint32_t(S), issued, issued_peer, slot_bytes, s.inject, unit,
                              s.ctl.timeout_ns);
     }
     if (PAIR == 2)

@@ -156,7 +156,7 @@ extern "C" int gemm_bias_relu_tf32_noalloc(const float* A, const float* B, const
     // One CTA per 128x256 tile: as many 48 KiB stages as fit beside the
     // epilogue staging (4 on GB300).
     int smax = 0;
-    while (smax < 16 && 1024 + size_t(smax + 1) * kUmmaStageBytes + kUmmaEpiBytes + 256 <=
+    while (smax < 16 && 1024 + size_t(smax + 1) * kUmmaStageBytes + kUmmaEpiBytes + kUmmaBarrierBytes <=
                             size_t(d->smem_optin))
         ++smax;
     if (stages < 1 || stages > smax) {

@@ -85,3 +85,35 @@ class split_tail:
         self.gbr.gemm_split_tail(-1)
         return False
 
+
+class thin_tail:
+    """Sets the grouped CTA-pair launches' thin tail tiles on or off for the
+    duration of a with-block, then restores the default (on)."""
+
+    def __init__(self, gbr, on):
+        self.gbr, self.on = gbr, on
+
+    def __enter__(self):
+        self.gbr.gemm_thin_tail(self.on)
+        return self
+
+    def __exit__(self, *exc):
+        self.gbr.gemm_thin_tail(True)
+        return False
+
+
+class ffma_warps:
+    """Selects the FFMA kernels' consumer layout (8 warps of 8x8, the default,
+    or 16 warps of 8x4) for the duration of a with-block, then restores the
+    default."""
+
+    def __init__(self, gbr, warps):
+        self.gbr, self.warps = gbr, warps
+
+    def __enter__(self):
+        self.gbr.ffma_tuning(self.warps)
+        return self
+
+    def __exit__(self, *exc):
+        self.gbr.ffma_tuning(-1)
+        return False

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from mbarrier_gemm_pipelines_gb300 import inputs
-from gpu_helpers import (TOL, load_library, rel_frobenius, require_gpu, split_tail,
+from gpu_helpers import (TOL, ffma_warps, load_library, rel_frobenius, require_gpu, split_tail,
                          to_host_f64, tuned)
 
 pytestmark = pytest.mark.gpu
@@ -64,6 +64,28 @@ def test_small_shapes(gbr, dtype, pair, M, N, K):
     with tuned(gbr, pair):
         got = _run(gbr, A, B, bias, dtype, 2)
     _check_full(got, A.float(), B.float(), bias, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["ffma", "ffma_cpasync", "ffma_sync"])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_ffma_layouts_agree(gbr, dtype, M, N, K):
+    """The FFMA consumer layouts (8 warps of 8x8, the default, and 16 warps
+    of 8x4) add each output's products in the same order: the same bits, and
+    parity with the oracle."""
+    A, B, bias = inputs.gemm_uniform(M, N, K, seed=M * 13 + N * 5 + K)
+    S = 1 if dtype == "ffma_sync" else 3
+    outs = []
+    for warps in (8, 16):
+        with ffma_warps(gbr, warps):
+            outs.append(_run(gbr, A, B, bias, dtype, S))
+    assert np.array_equal(outs[0], outs[1])
+    _check_full(outs[1], A, B, bias, "ffma")
+
+
+def test_ffma_tuning_is_validated(gbr):
+    with pytest.raises(gbr.GbrError):
+        gbr.ffma_tuning(12)
+    gbr.ffma_tuning(-1)
 
 
 @pytest.mark.parametrize("dtype,pair,ks", [v + (1,) for v in VARIANTS] +
@@ -124,6 +146,27 @@ def test_split_tail(gbr, dtype, pair, M, N, K):
             whole = _run(gbr, A, B, bias, dtype, 3)
     _check_full(got, A.float(), B.float(), bias, dtype)
     assert rel_frobenius(got, whole) <= TOL[dtype] / 10
+
+
+@pytest.mark.parametrize("dtype,pair,cols", [("bf16", 2, 16), ("bf16", 2, 3), ("bf16", 1, 5),
+                                            ("tf32", 2, 4)])
+def test_column_band_order(gbr, dtype, pair, cols):
+    """Tiles in bands of tile columns (row-major inside a band, the last band
+    narrower): the same bits as the default row-band order (each tile adds the
+    same products in the same order; split tail off), and parity with the
+    oracle.  2304 x 3328: 9-18 tile rows, 13 tile columns."""
+    A, B, bias = inputs.gemm_normal(2304, 3328, 320, seed=cols + pair)
+    if dtype == "bf16":
+        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    with tuned(gbr, pair), split_tail(gbr, 0):
+        base = _run(gbr, A, B, bias, dtype, 3)
+        gbr.gemm_raster_cols(cols)
+        try:
+            got = _run(gbr, A, B, bias, dtype, 3)
+        finally:
+            gbr.gemm_raster_cols(0)
+    assert np.array_equal(got, base)
+    _check_full(got, A.float(), B.float(), bias, dtype)
 
 
 def test_split_tail_mode_is_validated(gbr):
@@ -263,14 +306,16 @@ def _full_size(gbr, case, dtype, stages):
 
 
 @pytest.mark.parametrize("dtype,S,pair", [("ffma", 3, -1), ("ffma", 4, -1), ("ffma_cpasync", 4, -1),
-                                           ("tf32", 3, -1), ("tf32", 4, -1), ("tf32", 3, 1),
-                                           ("tf32", 4, 1)])
+                                           ("ffma16", 4, -1), ("tf32", 3, -1), ("tf32", 4, -1),
+                                           ("tf32", 3, 1), ("tf32", 4, 1)])
 def test_config3_fp32_4096(gbr, fp32_4096, dtype, S, pair):
     """fp32 4096^3, A, B ~ N(0,1)/sqrt(K), bias ~ N(0, 0.1), seed 2: strict fp32
-    FFMA (TMA or cp.async producer) and TF32 (CTA pair or one CTA per tile),
-    S in {3, 4}; every output element against the oracle."""
-    with tuned(gbr, pair):
-        _full_size(gbr, fp32_4096, dtype, S)
+    FFMA (TMA or cp.async producer; "ffma16": the 16-warp consumer layout) and
+    TF32 (CTA pair or one CTA per tile), S in {3, 4}; every output element
+    against the oracle."""
+    warps = 16 if dtype == "ffma16" else -1
+    with tuned(gbr, pair), ffma_warps(gbr, warps):
+        _full_size(gbr, fp32_4096, "ffma" if dtype == "ffma16" else dtype, S)
 
 
 @pytest.mark.parametrize("S,pair,ks", [(4, -1, -1), (5, -1, -1), (6, -1, -1), (4, 1, -1),

@@ -7,8 +7,8 @@ import torch
 
 import oracle
 from mbarrier_gemm_pipelines_gb300 import inputs
-from gpu_helpers import (TOL, load_library, rel_frobenius, require_gpu, split_tail, to_host_f64,
-                         tuned)
+from gpu_helpers import (TOL, load_library, rel_frobenius, require_gpu, split_tail, thin_tail,
+                         to_host_f64, tuned)
 
 pytestmark = pytest.mark.gpu
 
@@ -42,11 +42,12 @@ def test_grouped_small(gbr, counts, K, N, pair):
 @pytest.mark.parametrize("pair", [1, 2])
 def test_grouped_matches_dense_per_expert(gbr, pair):
     """Each expert's rows equal the dense kernel run on that expert alone (with
-    the split tail off both add the same products in the same order)."""
+    the split tail and the transposed thin tails off, both add the same
+    products in the same order)."""
     counts = [200, 77, 300]
     cnt, X, W, b = inputs.grouped(tokens=sum(counts), experts=3, K=256, N=512, seed=11)
     dX, dW, db = X.cuda(), W.cuda(), b.cuda()
-    with tuned(gbr, pair), split_tail(gbr, 0):
+    with tuned(gbr, pair), split_tail(gbr, 0), thin_tail(gbr, False):
         C = gbr.gemm_bias_relu_grouped(dX, dW, db, counts, stages=4)
         off = 0
         for e, n_e in enumerate(counts):
@@ -76,6 +77,53 @@ def test_grouped_split_tail(gbr, pair):
     assert rel_frobenius(got, ref) <= TOL["bf16"]
     assert np.abs(got - ref).max() <= 0.2 * np.abs(ref).max()
     assert rel_frobenius(got, to_host_f64(C0)) <= TOL["bf16"] / 10
+
+
+# Experts whose last 256-row tile holds 1, 16, 17, 100, 128 rows run it
+# transposed (thin); 129 and 255 rows do not; one expert is empty.
+THIN_COUNTS = [257, 272, 17, 100, 0, 128, 129, 511]
+
+
+@pytest.mark.parametrize("K,N", [(200, 520), (1024, 264)])
+def test_grouped_thin_tails(gbr, K, N):
+    """Thin tail tiles (C^T = W^T X^T on the CTA pair) against the oracle,
+    element by element, and against the same launch with every tile 256 rows
+    (agreement to the order of fp32 additions); ragged K and N."""
+    cnt, X, W, b = inputs.grouped(tokens=sum(THIN_COUNTS), experts=len(THIN_COUNTS), K=K, N=N,
+                                  seed=K + N)
+    dX, dW, db = X.cuda(), W.cuda(), b.cuda()
+    with tuned(gbr, 2):
+        C = gbr.gemm_bias_relu_grouped(dX, dW, db, THIN_COUNTS, stages=3)
+        with thin_tail(gbr, False):
+            C0 = gbr.gemm_bias_relu_grouped(dX, dW, db, THIN_COUNTS, stages=3)
+    gbr.check_device()
+    ref = oracle.gemm_bias_relu_grouped(X.float(), W.float(), b, THIN_COUNTS)
+    got = to_host_f64(C)
+    assert rel_frobenius(got, ref) <= TOL["bf16"]
+    assert np.abs(got - ref).max() <= 0.2 * np.abs(ref).max()
+    assert rel_frobenius(got, to_host_f64(C0)) <= TOL["bf16"] / 10
+    # the rows of the thin tiles on their own (every expert's last rows)
+    offs = oracle.group_offsets(THIN_COUNTS)
+    for e, n_e in enumerate(THIN_COUNTS):
+        t = n_e - 256 * ((n_e - 1) // 256) if n_e else 0
+        if 0 < t <= 128:
+            rows = slice(int(offs[e]) + n_e - t, int(offs[e]) + n_e)
+            assert rel_frobenius(got[rows], ref[rows]) <= TOL["bf16"], (e, t)
+
+
+def test_grouped_thin_tails_k_zero_and_switch(gbr):
+    cnt, X, W, b = inputs.grouped(tokens=sum(THIN_COUNTS), experts=len(THIN_COUNTS), K=64, N=264,
+                                  seed=5)
+    X0 = torch.empty((sum(THIN_COUNTS), 0), dtype=torch.bfloat16, device="cuda")
+    W0 = torch.empty((len(THIN_COUNTS), 0, 264), dtype=torch.bfloat16, device="cuda")
+    with tuned(gbr, 2):
+        C = gbr.gemm_bias_relu_grouped(X0, W0, b.cuda(), THIN_COUNTS, stages=3)
+    gbr.check_device()
+    ref = oracle.gemm_bias_relu_grouped(X0.cpu().float(), W0.cpu().float(), b, THIN_COUNTS)
+    expect = torch.from_numpy(ref).float().to(torch.bfloat16)
+    assert torch.equal(C.cpu(), expect)
+    from mbarrier_gemm_pipelines_gb300 import _binding as bnd
+    assert bnd.lib().gbr_gemm_thin_tail(2) == bnd.ERR_INVALID
 
 
 def test_grouped_rejects(gbr):
