@@ -247,17 +247,6 @@ int gbr_gemm_split_tail(int mode);
 int gbr_gemm_dynamic_schedule(int on);
 
 /*
- * Tile order of the dense tensor-core GEMM, for all later calls in the
- * process.  band_cols 0 (default): bands of gbr_gemm_tuning's group_m tile
- * rows, column-major inside a band.  band_cols > 0: bands of band_cols tile
- * columns, row-major inside a band, so that the units running at once share
- * the band's B column strips while A rows stream past.  Every tile adds the
- * same products either way; only the order of tiles, and so L2 reuse,
- * changes.  GBR_ERR_INVALID for a negative value.
- */
-int gbr_gemm_raster_cols(int band_cols);
-
-/*
  * Consumer layout of the strict-fp32 FFMA GEMM (GBR_F32_FFMA, its cp.async
  * variant and the homogeneous baseline's micro-tile), for all later calls in
  * the process.  consumer_warps 8 (-1: the default): 8 consumer warps (2 per

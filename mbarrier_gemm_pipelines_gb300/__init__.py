@@ -9,7 +9,7 @@ Operators (C ABI in ``include/gbr.h``; this package is a thin ctypes binding):
 """
 from ._binding import (BF16, F32_FFMA, F32_TF32, OP_COPY, OP_GEMM, GbrError, check, check_device,
                        copy_tuning, device_status, ffma_tuning, gemm_dynamic_schedule, gemm_split_tail,
-                       gemm_raster_cols, gemm_thin_tail, gemm_tuning, gemm_bias_relu, gemm_bias_relu_grouped,
+                       gemm_thin_tail, gemm_tuning, gemm_bias_relu, gemm_bias_relu_grouped,
                        gemm_bias_relu_host, launch_overlap,
                        last_error, launch_count, lib, library_path, max_stages,
                        gemm_bias_relu_tf32_noalloc, selftest_copy_skip_load, selftest_gemm_skip_load,
@@ -19,7 +19,7 @@ from ._build import build
 
 __all__ = [
     "BF16", "F32_FFMA", "F32_TF32", "OP_COPY", "OP_GEMM", "GbrError", "build", "check",
-    "check_device", "copy_tuning", "device_status", "ffma_tuning", "gemm_dynamic_schedule", "gemm_split_tail", "gemm_thin_tail", "gemm_raster_cols", "gemm_tuning", "gemm_bias_relu", "gemm_bias_relu_grouped", "gemm_bias_relu_host",
+    "check_device", "copy_tuning", "device_status", "ffma_tuning", "gemm_dynamic_schedule", "gemm_split_tail", "gemm_thin_tail", "gemm_tuning", "gemm_bias_relu", "gemm_bias_relu_grouped", "gemm_bias_relu_host",
     "last_error", "launch_count", "launch_overlap", "lib", "library_path", "max_stages", "selftest_copy_skip_load",
     "selftest_gemm_skip_load", "selftest_wait_timeout", "gemm_bias_relu_tf32_noalloc",
     "selftest_noalloc_skip_load",

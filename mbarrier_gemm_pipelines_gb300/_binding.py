@@ -42,7 +42,6 @@ SIGNATURES = {
     "gbr_launch_overlap": (_i32, [_i32]),
     "gbr_gemm_thin_tail": (_i32, [_i32]),
     "gbr_ffma_tuning": (_i32, [_i32]),
-    "gbr_gemm_raster_cols": (_i32, [_i32]),
     "gbr_trace_buffer": (_i32, [_vp, _u64]),
     "gbr_selftest_wait_timeout": (_i32, [_u64, _vp]),
     "gbr_selftest_gemm_skip_load": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32,
@@ -262,11 +261,6 @@ def gemm_split_tail(mode: int = -1) -> None:
 def gemm_dynamic_schedule(on: bool) -> None:
     """Tensor-core GEMM tiles from an atomic counter (True) or the static order (see gbr.h)."""
     check(lib().gbr_gemm_dynamic_schedule(int(bool(on))))
-
-
-def gemm_raster_cols(band_cols: int = 0) -> None:
-    """Dense tensor-core tile order: 0 row bands (default), n > 0 bands of n tile columns (see gbr.h)."""
-    check(lib().gbr_gemm_raster_cols(int(band_cols)))
 
 
 def ffma_tuning(consumer_warps: int = -1) -> None:

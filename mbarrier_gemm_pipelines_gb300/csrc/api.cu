@@ -38,7 +38,6 @@ int g_gemm_k_sub = -1;     // -1 auto (1): 128-byte K slices per ring stage
 int g_gemm_split = -1;     // -1 auto, 0 off, 1 on whenever some tile can be split
 int g_gemm_dynamic = 0;    // 1: tensor-core GEMMs take tiles from an atomic counter
 int g_gemm_thin = 1;       // 1: grouped CTA-pair launches run short last M-tiles transposed
-int g_gemm_group_n = 0;    // > 0: dense tensor-core tile order in bands of this many columns
 int g_launch_overlap = 1;  // 1: kernels are launched with programmatic stream serialization
 uint8_t* g_trace = nullptr;  // event trace buffer (device memory of the caller), or null
 uint32_t g_trace_cap = 0;    // records per (CTA, role)
@@ -467,14 +466,6 @@ int gbr_gemm_dynamic_schedule(int on) {
     return GBR_OK;
 }
 
-int gbr_gemm_raster_cols(int band_cols) {
-    if (band_cols < 0)
-        return fail(GBR_ERR_INVALID, "gbr_gemm_raster_cols: band_cols must be >= 0");
-    std::lock_guard<std::mutex> lk(g_mu);
-    g_gemm_group_n = band_cols;
-    return GBR_OK;
-}
-
 int gbr_ffma_tuning(int consumer_warps) {
     if (ffma_set_consumer_warps(consumer_warps < 0 ? 8 : consumer_warps) != 0)
         return fail(GBR_ERR_INVALID, "gbr_ffma_tuning: consumer_warps must be -1, 8 or 16");
@@ -819,10 +810,6 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
     s.num_kb = int32_t(cdiv(K, int64_t(bk) * s.k_sub));
     s.num_tiles = s.m_tiles * s.n_tiles;
     s.group_m = group_m_for(pair);
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        s.group_n = g_gemm_group_n;
-    }
     s.l2_hint = l2_hint_now();
     CUtensorMap ma, mb, mc;
     if ((r = encode_2d(&mc, dt, C, uint64_t(N), uint64_t(M), uint64_t(N) * es, panel_cols, 32,
@@ -1009,14 +996,10 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
             }
         }
     }
-    CUtensorMap mx, mx_thin, mw;
+    CUtensorMap mx, mw;
     if (K > 0) {
         if ((r = encode_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, uint64_t(K), uint64_t(T),
                            uint64_t(K) * es, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "X")) != GBR_OK)
-            return r;
-        if ((r = encode_2d(&mx_thin, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, uint64_t(K), uint64_t(T),
-                           uint64_t(K) * es, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B, "X thin")) !=
-            GBR_OK)
             return r;
         const uint64_t dims[3] = {uint64_t(N), uint64_t(K), uint64_t(num_groups)};
         const uint64_t strides[2] = {uint64_t(N) * es, uint64_t(K) * uint64_t(N) * es};
@@ -1026,7 +1009,6 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
             return r;
     } else {
         mx = mc[last_valid];
-        mx_thin = mc[last_valid];
         mw = mc[last_valid];
     }
     if ((r = check_umma_regs(*c, kUmmaBf16, true, pair)) != GBR_OK) return r;
@@ -1046,7 +1028,7 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
         if (ws) cudaFreeAsync(ws, st);
         return r;
     }
-    e = launch_gemm_umma_grouped(pair, mx, mx_thin, mw, mc, g, s, int64_t(N), grid, smem, st);
+    e = launch_gemm_umma_grouped(pair, mx, mw, mc, g, s, int64_t(N), grid, smem, st);
     if (ws) cudaFreeAsync(ws, st);
     if (dyn_ws) cudaFreeAsync(dyn_ws, st);
     if (e != cudaSuccess) return cuda_fail(e, "launching grouped GEMM");

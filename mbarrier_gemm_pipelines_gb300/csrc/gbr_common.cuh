@@ -184,21 +184,6 @@ __device__ __forceinline__ void raster_tile(uint32_t t, uint32_t m_tiles, uint32
     nt = r / rows;
 }
 
-// The transposed order: bands of `group_n` tile columns, row-major inside a
-// band.  Consecutive tiles walk across the band's columns, then down one row,
-// so the units running at once share the band's B strips while A rows stream
-// past.
-__device__ __forceinline__ void raster_tile_cols(uint32_t t, uint32_t m_tiles, uint32_t n_tiles,
-                                                 uint32_t group_n, uint32_t& mt, uint32_t& nt) {
-    const uint32_t band = group_n * m_tiles;
-    const uint32_t g = t / band;
-    const uint32_t first_n = g * group_n;
-    const uint32_t cols = min(group_n, n_tiles - first_n);
-    const uint32_t r = t - g * band;
-    nt = first_n + r % cols;
-    mt = r / cols;
-}
-
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }

@@ -73,8 +73,6 @@ struct GemmShape {
     int32_t num_tiles;
     int32_t stages;
     int32_t group_m;
-    int32_t group_n;               // tensor-core dense: > 0 bands of group_n tile columns
-                                   // (row-major inside), instead of group_m-row bands
     const float* bias;
     void* C;                       // used by epilogues that store with st.global
     const void* A;                 // read directly only by the cp.async producer variant
@@ -165,9 +163,7 @@ cudaError_t launch_gemm_umma(int kind, int pair, const CUtensorMap& mapA, const 
 cudaError_t launch_gemm_umma(int kind, const CUtensorMap& mapA, const CUtensorMap& mapB,
                              const CUtensorMap& mapC, const GemmShape& s, int grid, size_t smem,
                              cudaStream_t stream);
-// mapX_thin: X in boxes of 16 rows, read by thin tiles (GroupTable::thin).
-cudaError_t launch_gemm_umma_grouped(int pair, const CUtensorMap& mapX,
-                                     const CUtensorMap& mapX_thin, const CUtensorMap& mapW,
+cudaError_t launch_gemm_umma_grouped(int pair, const CUtensorMap& mapX, const CUtensorMap& mapW,
                                      const CUtensorMap* mapsC, const GroupTable& g,
                                      const GemmShape& s, int64_t bias_group_stride, int grid,
                                      size_t smem, cudaStream_t stream);

@@ -126,15 +126,13 @@ cudaError_t launch_gemm_umma(int kind, const CUtensorMap& mapA, const CUtensorMa
     return launch_gemm_umma(kind, 1, mapA, mapB, mapC, s, grid, smem, stream);
 }
 
-cudaError_t launch_gemm_umma_grouped(int pair, const CUtensorMap& mapX,
-                                     const CUtensorMap& mapX_thin, const CUtensorMap& mapW,
+cudaError_t launch_gemm_umma_grouped(int pair, const CUtensorMap& mapX, const CUtensorMap& mapW,
                                      const CUtensorMap* mapsC, const GroupTable& g,
                                      const GemmShape& s, int64_t bias_group_stride, int grid,
                                      size_t smem, cudaStream_t stream) {
     UmmaParams<true> P;
     memset(&P, 0, sizeof(P));
     P.mapA = mapX;
-    P.mapA_thin = mapX_thin;
     P.mapB = mapW;
     for (int e = 0; e < g.num_groups; ++e) P.mapC[e] = mapsC[e];
     P.s = s;

@@ -157,7 +157,6 @@ __device__ __forceinline__ void load_box_3d(uint32_t dst, const CUtensorMap* map
 template <bool GROUPED>
 struct UmmaParams {
     CUtensorMap mapA;
-    CUtensorMap mapA_thin;   // grouped: X in boxes of kThinBoxRows rows (thin tiles)
     CUtensorMap mapB;
     CUtensorMap mapC[GROUPED ? kMaxGroups : 1];
     GemmShape s;
@@ -172,20 +171,6 @@ struct TileInfo {
     int32_t group;
     int32_t thin;    // 0, or the rows of a transposed (thin) tile (its MMA N: rounded up to 16)
 };
-
-// A thin tile's X rows are loaded in boxes of this many rows (2 KiB of bf16
-// per 128-byte K slice), only as many as the tile uses.
-constexpr uint32_t kThinBoxRows = 16;
-
-// Bytes one CTA loads per ring stage of a tile: a thin tile's t rows need
-// n_pad / 2 rows of X per CTA, in ceil(n_pad / 2 / kThinBoxRows) boxes.
-template <int PAIR>
-__device__ __forceinline__ uint32_t cta_stage_bytes(int32_t thin, uint32_t ksub) {
-    if (thin <= 0) return ksub * Pair<PAIR>::stage_bytes;
-    const uint32_t rows = uint32_t((thin + 15) & ~15) / 2u;
-    const uint32_t boxes = (rows + kThinBoxRows - 1) / kThinBoxRows;
-    return ksub * (boxes * kThinBoxRows * 128u + Pair<PAIR>::b_bytes);
-}
 
 // Instruction descriptor of a thin tile (CTA pair, bf16): the MMA computes
 // C^T = W^T X^T, with A = W^T (the tile's 256 weight columns, MN-major: the
@@ -204,10 +189,7 @@ __device__ __forceinline__ TileInfo decode_tile(const UmmaParams<GROUPED>& P, ui
     ti.thin = 0;
     uint32_t mt, nt;
     if (!GROUPED) {
-        if (P.s.group_n > 0)
-            raster_tile_cols(t, P.s.m_tiles, P.s.n_tiles, P.s.group_n, mt, nt);
-        else
-            raster_tile(t, P.s.m_tiles, P.s.n_tiles, P.s.group_m, mt, nt);
+        raster_tile(t, P.s.m_tiles, P.s.n_tiles, P.s.group_m, mt, nt);
         ti.c_row = int32_t(mt * Pair<PAIR>::tile_m + rank * 128);
         ti.a_row = ti.c_row;
         ti.group = 0;
@@ -438,11 +420,9 @@ __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint32_t stage_base
 // Registrations are evened up first: the peer's half of an item it never
 // issued is counted done (complete_tx), and an item only the peer issued gets
 // the arrival and expect_tx of the peer's half.
-// Each producer records in slot_bytes[slot] the bytes its own copies of the
-// slot's latest item move (both CTAs of a pair move the same for an item).
 template <int PAIR>
 __device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t S, uint32_t issued,
-                                           uint32_t issued_peer, const uint32_t* slot_bytes,
+                                           uint32_t issued_peer, uint32_t cta_bytes,
                                            const FaultInjection& inj, uint32_t unit,
                                            uint64_t limit_ns) {
     const uint32_t hi = issued > issued_peer ? issued : issued_peer;
@@ -453,12 +433,8 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t S, uint32_t 
         const bool mine = j < issued, peer = PAIR == 2 && j < issued_peer;
         if (PAIR == 2) {
             if (!mine && !peer) continue;
-            if (mine && !peer) ptx::mbar_complete_tx(bar, slot_bytes[j % S]);
-            if (!mine && peer) {
-                const uint32_t peer_bytes = ptx::ld_shared_cluster_u32(
-                    ptx::mapa_shared(ptx::smem_addr(slot_bytes + j % S), 1));
-                ptx::mbar_arrive_expect_tx(bar, peer_bytes);
-            }
+            if (mine && !peer) ptx::mbar_complete_tx(bar, cta_bytes);
+            if (!mine && peer) ptx::mbar_arrive_expect_tx(bar, cta_bytes);
         } else if (!mine) {
             continue;
         }
@@ -500,7 +476,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tiles.empty = tiles.full + kTileRing;
     tiles.ids = reinterpret_cast<uint32_t*>(tiles.empty + kTileRing);
     uint32_t* issued_word = tiles.ids + kTileRing;   // ring items this CTA's producer issued
-    uint32_t* slot_bytes = issued_word + 1;          // [S]: bytes of this CTA's copies per slot
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const uint32_t rank = PAIR == 2 ? ptx::cluster_ctarank() : 0u;
@@ -573,10 +548,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                  ++j) {
                 const TileInfo ti = decode_tile<GROUPED, PAIR>(P, w.tile, rank);
                 const int32_t bcol0 = ti.n0 + int32_t(rank * PR::b_cols);
-                const bool thin = GROUPED && PAIR == 2 && ti.thin > 0;
-                const uint32_t my_bytes = cta_stage_bytes<PAIR>(thin ? ti.thin : 0, ksub);
-                const uint32_t thin_boxes =
-                    thin ? (uint32_t((ti.thin + 15) & ~15) / 2u + kThinBoxRows - 1) / kThinBoxRows : 0u;
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const uint32_t slot = it % S, ph = (it / S) & 1u;
                     if (!mbar_wait<kCl>(ptx::smem_addr(empty + slot), ph ^ 1u, s.ctl, abort_flag,
@@ -587,8 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (kTrace) trace_event(s.ctl, kRoleProducer, ntr, kEvWaitDone, it, slot, ph ^ 1u);
                     const uint32_t fb_local = ptx::smem_addr(full + slot);
                     const uint32_t fb = PAIR == 2 ? ptx::mapa_shared(fb_local, 0) : fb_local;
-                    slot_bytes[slot] = my_bytes;
-                    if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, PAIR * my_bytes);
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, PAIR * stage_bytes);
                     if (inject_skip_unit(s.inject, unit, it)) continue;   // self test
                     if (kTrace) trace_event(s.ctl, kRoleProducer, ntr, kEvIssued, it, slot, 0);
                     const uint32_t stage_base = ring_base + slot * stage_bytes;
@@ -598,14 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t b_dst =
                             stage_base + ksub * kUmmaAStageBytes + h * PR::b_bytes;
                         const int32_t k0 = (kb * int32_t(ksub) + int32_t(h)) * int32_t(K_::bk);
-                        if (GROUPED && PAIR == 2 && thin) {
-                            for (uint32_t i = 0; i < thin_boxes; ++i)
-                                load_box_2d<PAIR>(a_dst + i * kThinBoxRows * 128u, &P.mapA_thin, fb,
-                                                  k0, ti.a_row + int32_t(i * kThinBoxRows), hint,
-                                                  pol_a);
-                        } else {
-                            load_box_2d<PAIR>(a_dst, &P.mapA, fb, k0, ti.a_row, hint, pol_a);
-                        }
+                        load_box_2d<PAIR>(a_dst, &P.mapA, fb, k0, ti.a_row, hint, pol_a);
                         if (K_::b_kmajor) {
                             // Bt[N, K]: one box of this CTA's b_cols rows, 128 bytes of K each.
                             load_box_2d<PAIR>(b_dst, &P.mapB, fb, k0, bcol0, hint, pol_b);
@@ -875,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issued_peer = ptx::ld_shared_cluster_u32(ptx::mapa_shared(ptx::smem_addr(issued_word), 1));
         }
         if (aborted)
-            drain_ring<PAIR>(full, uint32_t(S), issued, issued_peer, slot_bytes, s.inject, unit,
+            drain_ring<PAIR>(full, uint32_t(S), issued, issued_peer, stage_bytes, s.inject, unit,
                              s.ctl.timeout_ns);
     }
     if (PAIR == 2)

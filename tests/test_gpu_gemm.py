@@ -148,27 +148,6 @@ def test_split_tail(gbr, dtype, pair, M, N, K):
     assert rel_frobenius(got, whole) <= TOL[dtype] / 10
 
 
-@pytest.mark.parametrize("dtype,pair,cols", [("bf16", 2, 16), ("bf16", 2, 3), ("bf16", 1, 5),
-                                            ("tf32", 2, 4)])
-def test_column_band_order(gbr, dtype, pair, cols):
-    """Tiles in bands of tile columns (row-major inside a band, the last band
-    narrower): the same bits as the default row-band order (each tile adds the
-    same products in the same order; split tail off), and parity with the
-    oracle.  2304 x 3328: 9-18 tile rows, 13 tile columns."""
-    A, B, bias = inputs.gemm_normal(2304, 3328, 320, seed=cols + pair)
-    if dtype == "bf16":
-        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
-    with tuned(gbr, pair), split_tail(gbr, 0):
-        base = _run(gbr, A, B, bias, dtype, 3)
-        gbr.gemm_raster_cols(cols)
-        try:
-            got = _run(gbr, A, B, bias, dtype, 3)
-        finally:
-            gbr.gemm_raster_cols(0)
-    assert np.array_equal(got, base)
-    _check_full(got, A.float(), B.float(), bias, dtype)
-
-
 def test_split_tail_mode_is_validated(gbr):
     with pytest.raises(gbr.GbrError):
         gbr.gemm_split_tail(2)
