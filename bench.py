@@ -31,7 +31,7 @@ if ROOT not in sys.path:
 METRIC = "TFLOP/s of ReLU(A·B+bias) and GB/s of TMA staged copy, as % of GB300 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_FILES = ["gbr_ptx.cuh", "gbr_common.cuh", "gbr_internal.h", "gemm_umma.cuh",
-                "split_plan.cuh", "staged_copy.cu", "gemm_ffma.cu", "transpose.cu"]
+                "split_plan.cuh", "staged_copy.cu", "gemm_ffma.cu"]
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -344,7 +344,7 @@ def measure_workloads(gbr, peaks, sm_mhz=None, steps=20, warmup=3):
     for dt, peak, bound, unit, stage_list in (
             ("ffma", fp32_alu_peak, "alu", "FP32 FMA lanes: 152 SM x 128 x 2 x f_SM", (3, 4)),
             ("tf32", bf16_peak * 0.5, "tensor",
-             "measured bf16 x 0.5 (nominal TF32:bf16 dense ratio); includes the B transpose pass",
+             "measured bf16 x 0.5 (nominal TF32:bf16 dense ratio); B read in place, MN-major",
              (3, 4))):
         for S in stage_list:
             v, ms = timed(lambda: gbr.gemm_bias_relu(dA, dB, db, dC, dtype=dt, stages=S), f)

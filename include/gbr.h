@@ -30,7 +30,7 @@
  *     bf16 row lengths a multiple of 8.  Otherwise GBR_ERR_ALIGN.
  *   - The library keeps, per device, a 64-byte status block it allocates on
  *     first use, a memory pool for per-call scratch (taken and returned in
- *     stream order: the TF32 Bt copy, split-tile sums, the tile counter), the
+ *     stream order: split-tile sums, the dynamic tile counter), the
  *     streams and events of gemm_bias_relu_host, and cached device attributes.
  */
 #ifndef GBR_H_
@@ -274,7 +274,7 @@ int gbr_gemm_thin_tail(int on);
 
 /*
  * Programmatic dependent launch of the library's pipeline kernels (the
- * staged copy, the FFMA and tensor-core GEMMs and the TF32 B transpose), for
+ * staged copy, the FFMA and tensor-core GEMMs), for
  * all later calls in the process.  on = 1 (default): each is launched so that
  * it may be scheduled before the previous kernel in the stream has finished;
  * its CTAs set up their barriers and Tensor Memory, then wait
@@ -373,17 +373,16 @@ int gbr_selftest_copy_skip_load(const void *src, void *dst, int64_t rows, int64_
  * or synchronise the device at unpredictable times), plug-ins whose host
  * framework owns all device allocation, and processes whose device memory is
  * entirely reserved by another allocator, so that an allocation from this
- * library would fail.  This variant takes a K-major copy of B (K*N*4 bytes,
- * made by a transpose kernel) and its status words from one file-scope
- * device array of 16 MiB + 256 bytes, which the CUDA driver creates on every
- * device that loads this library and keeps until the process exits.  The call
- * allocates nothing, and neither does gbr_device_status().
+ * library would fail.  It runs the TF32 tensor-core kernel with one CTA per
+ * tile and no split (so it needs no per-call scratch) and takes its status
+ * words from one file-scope device array of 256 bytes, which the CUDA driver
+ * creates on every device that loads this library and keeps until the process
+ * exits.  The call allocates nothing, and neither does gbr_device_status().
  *
  *   A [M, K], B [K, N], bias [N], C [M, N]: fp32, as for gemm_bias_relu;
  *   caller-owned device memory.  K and N multiples of 4.  C must not overlap
  *   A, B or bias (GBR_ERR_INVALID).
- *   K * N must be <= 4194304 (K*N*4 bytes <= 16 MiB): larger sizes return
- *   GBR_ERR_INVALID without launching anything.
+ *   M, N, K < 2^31 (GBR_ERR_INVALID otherwise, nothing launched).
  *   stages: 1..4 -- this call always runs one CTA per 128x256 tile, whose
  *   ring holds 4 stages on GB300; gbr_max_stages() reports the CTA-pair
  *   kernel's larger limit, which does not apply here (GBR_ERR_SMEM).

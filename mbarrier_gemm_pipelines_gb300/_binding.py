@@ -338,10 +338,10 @@ def gemm_bias_relu_tf32_noalloc(A, B, bias, C, stages=4, stream=None):
 
     For callers that may not allocate: serving loops that must stay out of
     allocators, plug-ins whose host framework owns all device allocation,
-    processes whose device memory is reserved by another allocator.  Scratch
-    comes from a fixed 16 MiB device array that every call on the device
-    shares (K * N <= 4194304); calls that overlap on the GPU race, so
-    serialise them.  One CTA per tile: stages 1..4."""
+    processes whose device memory is reserved by another allocator.  Its
+    status words live in a fixed device array that every call on the device
+    shares; calls that overlap on the GPU race, so serialise them.  One CTA
+    per tile, never split: stages 1..4."""
     M, N, K = _noalloc_shapes(A, B, bias, C)
     check(lib().gemm_bias_relu_tf32_noalloc(A.data_ptr(), B.data_ptr(), bias.data_ptr(),
                                             C.data_ptr(), M, N, K, int(stages),

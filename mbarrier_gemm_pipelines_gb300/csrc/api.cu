@@ -135,8 +135,8 @@ int get_ctx(DevCtx** out, int* dev_out = nullptr) {
             return cuda_fail(e, "cudaMalloc(status block)");
         if ((e = cudaMemset(c.status, 0, kStatusWords * sizeof(uint32_t))) != cudaSuccess)
             return cuda_fail(e, "cudaMemset(status block)");
-        // A pool of this library's own for per-call scratch (the TF32 B
-        // transpose, split-tile partial sums): allocation and release are
+        // A pool of this library's own for per-call scratch (split-tile
+        // partial sums, the dynamic tile counter): allocation and release are
         // stream-ordered, so calls on different streams never share scratch,
         // and the pool keeps the memory it has mapped for the next call.
         cudaMemPoolProps props;
@@ -823,33 +823,29 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
     const size_t split_bytes =
         dynamic_wanted(s) ? 0 : plan_split(s, units, umma_split_scratch(pair));
     const int grid = pair * int(split_bytes ? units : std::min<int64_t>(s.num_tiles, units));
-    float* bt = nullptr;  // TF32 only: K-major copy of B, stream-ordered scratch
     if (K > 0) {
         if ((r = encode_2d(&ma, dt, A, uint64_t(K), uint64_t(M), uint64_t(K) * es, bk, 128,
                            CU_TENSOR_MAP_SWIZZLE_128B, "A")) != GBR_OK)
             return r;
-        if (kind == kUmmaBf16) {
-            // B row-major [K, N] as N-major panels of panel_cols x bk (MN-major operand).
-            if ((r = encode_2d(&mb, dt, B, uint64_t(N), uint64_t(K), uint64_t(N) * es, panel_cols,
-                               bk, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != GBR_OK)
-                return r;
+        // B row-major [K, N] as N-major panels of panel_cols x bk (MN-major
+        // operand); TF32 panels in the 32-byte-atom swizzle kind::tf32 reads.
+        // When N is a whole number of panels, B is seen as a 3-D tensor
+        // (column in panel, K, panel), so that one box brings all of a CTA's
+        // panels of a K slice, laid out panel after panel; its addresses stay
+        // inside B because every panel is whole.
+        const CUtensorMapSwizzle swz =
+            kind == kUmmaTf32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
+        s.b_panels_3d = N % int64_t(panel_cols) == 0 ? 1u : 0u;
+        if (s.b_panels_3d) {
+            const uint64_t dims[3] = {panel_cols, uint64_t(K), uint64_t(N) / panel_cols};
+            const uint64_t strides[2] = {uint64_t(N) * es, uint64_t(panel_cols) * es};
+            const uint32_t box[3] = {panel_cols, bk, uint32_t(kUmmaBN / pair) / panel_cols};
+            r = encode(&mb, dt, 3, B, dims, strides, box, swz, "B panels");
         } else {
-            if ((e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&bt),
-                                             size_t(K) * size_t(N) * 4, c->pool, st)) != cudaSuccess)
-                return cuda_fail(e, "cudaMallocFromPoolAsync(TF32 B transpose)");
-            if ((r = encode_2d(&mb, dt, bt, uint64_t(K), uint64_t(N), uint64_t(K) * es, bk,
-                               uint32_t(kUmmaBN / pair), CU_TENSOR_MAP_SWIZZLE_128B,
-                               "Bt")) != GBR_OK) {
-                cudaFreeAsync(bt, st);
-                return r;
-            }
-            if ((e = launch_transpose_f32(static_cast<const float*>(B), bt, int(K), int(N), st)) !=
-                cudaSuccess) {
-                cudaFreeAsync(bt, st);
-                return cuda_fail(e, "launching the B transpose");
-            }
-            ++g_launches;
+            r = encode_2d(&mb, dt, B, uint64_t(N), uint64_t(K), uint64_t(N) * es, panel_cols, bk,
+                          swz, "B");
         }
+        if (r != GBR_OK) return r;
     } else {
         ma = mc;  // never read: no k-blocks are loaded when K == 0
         mb = mc;
@@ -859,13 +855,11 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
     if ((r = split_scratch(*c, s, umma_split_scratch(pair), split_bytes, st, &ws)) != GBR_OK ||
         (r = dynamic_scratch(*c, s, st, &dyn_ws)) != GBR_OK) {
         if (ws) cudaFreeAsync(ws, st);
-        if (bt) cudaFreeAsync(bt, st);
         return r;
     }
     e = launch_gemm_umma(kind, pair, ma, mb, mc, s, grid, smem, st);
     if (ws) cudaFreeAsync(ws, st);
     if (dyn_ws) cudaFreeAsync(dyn_ws, st);
-    if (bt) cudaFreeAsync(bt, st);
     if (e != cudaSuccess) return cuda_fail(e, "launching tcgen05 GEMM");
     ++g_launches;
     return GBR_OK;

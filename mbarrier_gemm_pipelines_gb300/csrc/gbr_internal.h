@@ -79,6 +79,9 @@ struct GemmShape {
     const void* B;
     KernelCtl ctl;
     uint32_t k_sub;                // tensor-core GEMM: 128-byte K slices per ring stage (1, 2)
+    uint32_t b_panels_3d;          // dense tensor-core GEMM: 1 when mapB is 3-D (column in
+                                   // panel, K, panel), one box per K slice for all of this
+                                   // CTA's B panels; 0: one 2-D box per panel
     uint32_t l2_hint;              // tensor-core GEMM operand loads: 0 none, 1 A and B
                                    // evict_last, 2 A evict_first / B evict_last,
                                    // 3 A evict_last / B evict_first, 4 both evict_normal
@@ -131,8 +134,8 @@ constexpr uint32_t kUmmaEpiBytes = 4 * 2 * 32 * 128;        // 4 warps x 2 buffe
 constexpr uint32_t kUmmaBarrierBytes = 384;
 constexpr int kMaxGroups = 32;
 
-// bf16 (B read MN-major from B[K, N]); TF32 (B read K-major from a transposed
-// copy Bt[N, K] that a pre-pass kernel writes).
+// Operand types of the tensor-core GEMM; both read A K-major from A[M, K] and
+// B MN-major from B[K, N].
 enum UmmaKind : int { kUmmaBf16 = 0, kUmmaTf32 = 1 };
 constexpr int kUmmaKinds = 2;
 
@@ -169,7 +172,6 @@ cudaError_t launch_gemm_umma_grouped(int pair, const CUtensorMap& mapX, const CU
                                      size_t smem, cudaStream_t stream);
 
 // Bt[N, K] = B[K, N], 32-bit elements, K and N multiples of 4.
-cudaError_t launch_transpose_f32(const float* B, float* Bt, int K, int N, cudaStream_t stream);
 
 // ------------------------------------------------------------ no-alloc variant
 // Status words of the no-alloc scratch on the current device: returns the error

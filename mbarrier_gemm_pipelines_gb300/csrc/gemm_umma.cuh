@@ -45,11 +45,11 @@
 //
 // Shared-memory ring stage (every kind: 128 bytes of K per row):
 //   A: 128 rows (M) x 128 B, K-major, TMA 128-byte swizzle      16 KiB
-//   B: 256 / PAIR columns of this CTA:
-//      bf16: N-major panels of 64 rows (K) x 128 B (64 columns)  8 KiB each
-//      tf32: K-major, one 128-byte row of K per column, loaded from a
-//            transposed copy Bt[N, K] that a pre-pass kernel writes (an
-//            MN-major TF32 operand is not usable: see sw128_desc)
+//   B: 256 / PAIR columns of this CTA, N-major panels of 128 B of N read
+//      straight from B[K, N] (MN-major operand):
+//      bf16: 64 rows (K) x 64 columns, TMA 128-byte swizzle       8 KiB each
+//      tf32: 32 rows (K) x 32 columns, TMA 128-byte swizzle with
+//            32-byte atoms (the only MN-major form kind::tf32 reads)  4 KiB each
 //   PAIR = 1: 48 KiB per stage, PAIR = 2: 32 KiB per stage.
 // kind     BK  MMA K
 // bf16     64   16
@@ -71,6 +71,9 @@ constexpr uint32_t kRegsWG0 = 88;
 constexpr uint32_t kRegsWG1 = 224;
 constexpr uint32_t kEpiBufBytes = 32 * 128;   // 32 rows x 128 B per warp buffer
 
+// Layout field of a shared-memory matrix descriptor (see sw128_desc).
+constexpr uint32_t kDescSw128 = 2, kDescSw128Atom32 = 1;
+
 template <int KIND>
 struct Kind;
 template <>
@@ -78,14 +81,16 @@ struct Kind<kUmmaBf16> {
     static constexpr uint32_t esize = 2, bk = 64, mma_k = 16, panel_cols = 64;
     static constexpr uint32_t ab_format = 1;          // BF16
     static constexpr uint32_t out_chunk_cols = 64;    // 64 bf16 = 128 B per row
-    static constexpr bool b_kmajor = false;           // B stays row-major [K, N]
+    // MN-major B: 128-byte swizzle, 8-row K groups 1024 B apart.
+    static constexpr uint32_t b_layout = kDescSw128, b_sbo = 1024;
 };
 template <>
 struct Kind<kUmmaTf32> {
     static constexpr uint32_t esize = 4, bk = 32, mma_k = 8, panel_cols = 32;
     static constexpr uint32_t ab_format = 2;          // TF32
     static constexpr uint32_t out_chunk_cols = 32;    // 32 fp32 = 128 B per row
-    static constexpr bool b_kmajor = true;            // B arrives transposed, Bt[N, K]
+    // MN-major B: 128-byte swizzle of 32-byte atoms, 4-row K groups 512 B apart.
+    static constexpr uint32_t b_layout = kDescSw128Atom32, b_sbo = 512;
 };
 
 template <int PAIR>
@@ -97,35 +102,38 @@ struct Pair {
 };
 
 // Instruction descriptor, kind::f16 / kind::tf32: fp32 accumulator, A K-major,
-// B MN-major (bf16) or K-major (tf32), M = 128 * PAIR, N = 256, dense.
+// B MN-major, M = 128 * PAIR, N = 256, dense.
 template <int KIND, int PAIR>
 __host__ __device__ constexpr uint32_t make_idesc() {
     return (1u << 4)                                     // D format: f32
            | (Kind<KIND>::ab_format << 7)                // A format
            | (Kind<KIND>::ab_format << 10)               // B format
            | (0u << 15)                                  // A: K-major
-           | ((Kind<KIND>::b_kmajor ? 0u : 1u) << 16)    // B: K-major / MN-major
+           | (1u << 16)                                  // B: MN-major
            | ((uint32_t(kUmmaBN) >> 3) << 17)            // N / 8
            | ((Pair<PAIR>::tile_m >> 4) << 24);          // M / 16
 }
 
-// Shared-memory matrix descriptor with 128-byte swizzling.
+// Shared-memory matrix descriptor, 128-byte rows.
 //   bits  0-13 start address >> 4     bits 16-29 leading byte offset >> 4
 //   bits 32-45 stride byte offset >> 4  bits 46-48 = 0b001 (tcgen05 version)
 //   bits 49-51 base offset = 0 (atoms are 1024-byte aligned)
-//   bits 61-63 = 2 (128-byte swizzle)
-// K-major operand (A; TF32 B): rows 128 B apart, 8-row groups SBO = 1024 B
-// apart, LBO unused; the k-th MMA of a stage starts k * 32 bytes into the row.
-// MN-major B (bf16): 8 K-rows of 128 B form a 1024-byte atom (64 columns),
-// atoms along K are SBO = 1024 B apart and 128-byte column panels are LBO =
-// panel bytes apart; the k-th MMA of a stage starts k * 16 rows into the panel.
-// kind::tf32 does not take an MN-major B on this part: with the same
-// descriptor scheme, panels of 32 fp32 columns, K advance of 8 rows and the
-// transpose-B bit set, the MMA wrote exact zeros over the whole tile (B all
-// ones included), so TF32 reads B K-major from a transposed copy.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+//   bits 61-63 layout: 2 = 128-byte swizzle (16-byte atoms),
+//                      1 = 128-byte swizzle of 32-byte atoms
+// K-major operand (A): rows 128 B apart, 8-row groups SBO = 1024 B apart, LBO
+// unused; the k-th MMA of a stage starts k * 32 bytes into the row.
+// MN-major B: each K row of a panel holds 128 B of N; K groups are SBO apart
+// (bf16: 8 rows, 1024 B; tf32: 4 rows, 512 B) and 128-byte column panels LBO
+// = panel bytes apart; the k-th MMA of a stage starts k * MMA-K rows into the
+// panel.  kind::tf32 reads an MN-major operand only in the 32-byte-atom form
+// (which TMA writes with CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B): measured on
+// GB300, the same panels in the 16-byte-atom form give exact zeros, and with
+// 32-byte atoms and 8-row groups the rows of each group come out permuted.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                               uint32_t layout = kDescSw128) {
     return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
-           (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+           (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) |
+           (uint64_t(layout) << 61);
 }
 
 // TMA loads of one operand box, one CTA or the CTA pair, with or without an
@@ -385,9 +393,8 @@ __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint32_t stage_base
 #pragma unroll
         for (uint32_t k = 0; k < 128 / (K_::mma_k * K_::esize); ++k) {
             const uint64_t ad = sw128_desc(a_base + k * K_::mma_k * K_::esize, 16, 1024);
-            const uint64_t bd = K_::b_kmajor
-                                    ? sw128_desc(b_base + k * K_::mma_k * K_::esize, 16, 1024)
-                                    : sw128_desc(b_base + k * K_::mma_k * 128, kPanelBytes, 1024);
+            const uint64_t bd = sw128_desc(b_base + k * K_::mma_k * 128, kPanelBytes,
+                                           K_::b_sbo, K_::b_layout);
             const uint32_t acc = (!first || h != 0 || k != 0) ? 1u : 0u;
             if (PAIR == 2) {
                 if (KIND == kUmmaBf16) {
@@ -569,16 +576,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             stage_base + ksub * kUmmaAStageBytes + h * PR::b_bytes;
                         const int32_t k0 = (kb * int32_t(ksub) + int32_t(h)) * int32_t(K_::bk);
                         load_box_2d<PAIR>(a_dst, &P.mapA, fb, k0, ti.a_row, hint, pol_a);
-                        if (K_::b_kmajor) {
-                            // Bt[N, K]: one box of this CTA's b_cols rows, 128 bytes of K each.
-                            load_box_2d<PAIR>(b_dst, &P.mapB, fb, k0, bcol0, hint, pol_b);
+                        if (!GROUPED && s.b_panels_3d) {
+                            // All of this CTA's panels of the slice in one box.
+                            load_box_3d<PAIR>(b_dst, &P.mapB, fb, 0, k0,
+                                              bcol0 / int32_t(K_::panel_cols), hint, pol_b);
                         } else {
 #pragma unroll
                             for (uint32_t j = 0; j < PR::b_cols / K_::panel_cols; ++j) {
                                 const int32_t n = bcol0 + int32_t(j * K_::panel_cols);
                                 const uint32_t d = b_dst + j * kPanelBytes;
                                 if (GROUPED)
-                                    load_box_3d<PAIR>(d, &P.mapB, fb, n, k0, ti.group, hint, pol_b);
+                                    load_box_3d<PAIR>(d, &P.mapB, fb, n, k0, ti.group, hint,
+                                                      pol_b);
                                 else
                                     load_box_2d<PAIR>(d, &P.mapB, fb, n, k0, hint, pol_b);
                             }

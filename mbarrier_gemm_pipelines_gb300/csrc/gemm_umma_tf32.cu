@@ -1,4 +1,4 @@
-// gemm_umma_tf32.cu -- the tensor-core GEMM instances for TF32 (B read K-major from a transposed copy Bt)
+// gemm_umma_tf32.cu -- the tensor-core GEMM instances for TF32 (B read MN-major from B[K, N])
 // (every CTA-pair mode, K slices per stage and trace/dynamic mode).
 #include "gemm_umma.cuh"
 

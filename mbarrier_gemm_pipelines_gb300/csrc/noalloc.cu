@@ -1,18 +1,17 @@
 // noalloc.cu -- the TF32 GEMM + bias + ReLU for callers that cannot allocate
 // device memory.
 //
-// The regular TF32 entry point needs K*N*4 bytes of scratch for the K-major
-// copy of B, which it takes from the stream-ordered allocator on every call,
-// plus the library's per-device status block, which it allocates on first use.
-// Some callers cannot do either: serving loops that must never enter an
-// allocator (it can take locks or synchronise the device at unpredictable
-// times), plug-ins whose host framework owns all device allocation, and
-// processes whose device memory is entirely reserved by another allocator, so
-// that a cudaMalloc or cudaMallocAsync from this library would fail.  This
-// variant runs the same two kernels (B transpose, then the tcgen05 TF32 GEMM)
-// but takes all its scratch -- status words and the transposed B -- from one
-// file-scope device array that the CUDA driver creates when the library's
-// module is loaded.
+// The regular entry point allocates the library's per-device status block on
+// first use, and may take per-call scratch from the stream-ordered allocator
+// (split-tile partial sums, the dynamic tile counter).  Some callers cannot
+// allow either: serving loops that must never enter an allocator (it can take
+// locks or synchronise the device at unpredictable times), plug-ins whose host
+// framework owns all device allocation, and processes whose device memory is
+// entirely reserved by another allocator, so that a cudaMalloc or
+// cudaMallocAsync from this library would fail.  This variant runs the TF32
+// tensor-core GEMM kernel, one CTA per tile and never split, and takes its
+// only scratch -- the status words -- from a file-scope device array that the
+// CUDA driver creates when the library's module is loaded.
 #include "gbr.h"
 #include "gbr_internal.h"
 
@@ -28,8 +27,7 @@ namespace gbr {
 namespace {
 
 constexpr size_t kNoallocStatusBytes = 256;             // kStatusWords words, padded
-constexpr size_t kNoallocBtBytes = size_t(16) << 20;    // largest K*N*4 accepted
-constexpr size_t kNoallocScratchBytes = kNoallocStatusBytes + kNoallocBtBytes;
+constexpr size_t kNoallocScratchBytes = kNoallocStatusBytes;
 
 // Held by every device that loads this library until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
@@ -60,7 +58,8 @@ PFN_cuTensorMapEncodeTiled_v12000 na_encode_fn() {
 }
 
 bool na_map_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
-               uint32_t box_inner, uint32_t box_outer) {
+               uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = na_encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -68,7 +67,22 @@ bool na_map_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t es[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box,
-              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// B [K, N] fp32 as a 3-D tensor (column in a 32-column panel, K, panel), for
+// N a multiple of 32: one box brings the 8 panels of a 32-row K slice of a
+// 256-column tile, in the 32-byte-atom swizzle that the TF32 MMA reads.
+bool na_map_b_panels(CUtensorMap* map, const void* B, uint64_t K, uint64_t N) {
+    auto fn = na_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {32, K, N / 32};
+    cuuint64_t strides[2] = {N * 4, 128};
+    cuuint32_t box[3] = {32, 32, 8};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(B), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -146,10 +160,6 @@ extern "C" int gemm_bias_relu_tf32_noalloc(const float* A, const float* B, const
     const int64_t lim = int64_t(1) << 31;
     if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim)
         return report_error(GBR_ERR_INVALID, "gemm_bias_relu_tf32_noalloc: M, N, K must be in [0, 2^31)");
-    if (uint64_t(K) * uint64_t(N) * 4u > kNoallocBtBytes)
-        return report_error(GBR_ERR_INVALID,
-                            "gemm_bias_relu_tf32_noalloc: K*N*4 bytes exceeds the 16 MiB no-alloc "
-                            "scratch (K*N must be <= 4194304); use gemm_bias_relu");
     NoallocDevice* d;
     int r = na_setup(&d);
     if (r != GBR_OK) return r;
@@ -189,10 +199,8 @@ extern "C" int gemm_bias_relu_tf32_noalloc(const float* A, const float* B, const
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // Status words: zero at set-up and after every read that found a timeout,
     // so a recorded timeout stays until gbr_device_status() reads it (the
-    // first one recorded is the one kept).  Bt: fully rewritten by the
-    // transpose of every call, so it needs no clearing.
+    // first one recorded is the one kept).
     uint32_t* status = reinterpret_cast<uint32_t*>(d->scratch);
-    float* bt = reinterpret_cast<float*>(d->scratch + kNoallocStatusBytes);
 
     GemmShape s;
     memset(&s, 0, sizeof(s));
@@ -214,8 +222,14 @@ extern "C" int gemm_bias_relu_tf32_noalloc(const float* A, const float* B, const
     if (!na_map_2d(&mc, C, uint64_t(N), uint64_t(M), 32, 32))
         return report_error(GBR_ERR_INVALID, "encoding the C tensor map failed");
     if (K > 0) {
+        // A K-major; B as N-major panels of 32 columns x 32 K rows in the
+        // 32-byte-atom swizzle that the TF32 MMA reads (one box per panel, or
+        // one per K slice when N is a whole number of panels).
+        s.b_panels_3d = N % 32 == 0 ? 1u : 0u;
         if (!na_map_2d(&ma, A, uint64_t(K), uint64_t(M), 32, 128) ||
-            !na_map_2d(&mb, bt, uint64_t(K), uint64_t(N), 32, 256))
+            !(s.b_panels_3d ? na_map_b_panels(&mb, B, uint64_t(K), uint64_t(N))
+                            : na_map_2d(&mb, B, uint64_t(N), uint64_t(K), 32, 32,
+                                        CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)))
             return report_error(GBR_ERR_INVALID, "encoding the A/B tensor maps failed");
     } else {
         ma = mc;
@@ -224,11 +238,6 @@ extern "C" int gemm_bias_relu_tf32_noalloc(const float* A, const float* B, const
     const size_t smem = umma_smem_bytes(stages);
     if (umma_prepare(kUmmaTf32, false, smem) != cudaSuccess)
         return report_error(GBR_ERR_CUDA, "cudaFuncSetAttribute(tcgen05 GEMM) failed");
-    if (K > 0) {
-        if (launch_transpose_f32(B, bt, int(K), int(N), st) != cudaSuccess)
-            return report_error(GBR_ERR_CUDA, "launching the B transpose failed");
-        count_launch();
-    }
     const int grid = int(std::min<int64_t>(s.num_tiles, d->sm_count));
     if (launch_gemm_umma(kUmmaTf32, ma, mb, mc, s, grid, smem, st) != cudaSuccess)
         return report_error(GBR_ERR_CUDA, "launching the tcgen05 GEMM failed");

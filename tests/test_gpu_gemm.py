@@ -124,6 +124,27 @@ def test_pair_and_single_agree(gbr, dtype):
     _check_full(outs[1], A.float(), B.float(), bias, dtype)
 
 
+@pytest.mark.parametrize("dtype", ["tf32", "bf16"])
+@pytest.mark.parametrize("pair", [1, 2])
+def test_b_panel_boxes_agree(gbr, dtype, pair):
+    """B loaded as one 3-D box of whole panels per K slice (N a multiple of
+    the panel width) and as one 2-D box per panel (N ragged: the same B with
+    8 zero columns appended) gives the same bits in the shared columns; both
+    match the oracle.  N = 1536 makes the last tile's CTAs reach past N (its
+    boxes zero-fill whole panels)."""
+    M, N, K = 384, 1536, 392
+    A, B, bias = inputs.gemm_normal(M, N, K, seed=9)
+    Bpad = torch.cat([B, torch.zeros(K, 8)], dim=1)
+    biaspad = torch.cat([bias, torch.zeros(8)])
+    if dtype == "bf16":
+        A, B, Bpad = A.to(torch.bfloat16), B.to(torch.bfloat16), Bpad.to(torch.bfloat16)
+    with tuned(gbr, pair), split_tail(gbr, 0):   # the two tile counts would split differently
+        whole = _run(gbr, A, B, bias, dtype, 3)
+        ragged = _run(gbr, A, Bpad, biaspad, dtype, 3)
+    assert np.array_equal(whole, ragged[:, :N])
+    _check_full(whole, A.float(), B.float(), bias, dtype)
+
+
 # Tile counts that leave a partial last round of units, K long enough to split:
 # a few tiles only (every unit runs a split run), more tiles than units (whole
 # tiles first, then the split round), ragged edges in M and N.

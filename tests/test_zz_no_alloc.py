@@ -1,9 +1,9 @@
 """gemm_bias_relu_tf32_noalloc -- the TF32 GEMM + bias + ReLU for callers that
 cannot allocate device memory (serving loops that must stay out of allocators,
 plug-ins whose host framework owns device allocation, processes whose device
-memory is reserved by another allocator).  Its scratch is a fixed device array
-inside the library that every call on the device reuses, so its output is
-checked against the binary64 oracle call after call, at the TF32 bar.
+memory is reserved by another allocator).  Its status words sit in a fixed
+device array inside the library that every call on the device reuses, so its
+output is checked against the binary64 oracle call after call, at the TF32 bar.
 
 Collected last (file name) so that a run stopping at the first failure has
 already run every other test; it also passes on its own in a fresh process,
@@ -41,8 +41,8 @@ def test_noalloc_matches_oracle_twice():
     gbr = load_library()
     from mbarrier_gemm_pipelines_gb300 import _binding as b
     lib = b.lib()
-    # Two calls in a row with different shapes: the second reuses the scratch
-    # array the first one left behind (a larger K-major B copy, then a smaller one).
+    # Two calls in a row with different shapes: the second reuses the status
+    # words the first one left behind.
     for M, N, K, seed in [(640, 1024, 2048, 22), (300, 520, 200, 21)]:
         A, B, bias = inputs.gemm_normal(M, N, K, seed=seed)
         C = torch.full((M, N), float("nan"), device="cuda")
@@ -51,19 +51,25 @@ def test_noalloc_matches_oracle_twice():
         _check_oracle(C, A, B, bias)
 
 
-def test_noalloc_rejects_sizes_beyond_its_scratch():
+def test_noalloc_large_b_and_index_limit():
+    """B of 2052 x 2048 fp32 (16.0 MiB, read in place: no copy of it is made),
+    against the oracle; sizes of 2^31 or more are rejected with nothing
+    launched."""
     require_gpu()
-    load_library()
+    gbr = load_library()
     from mbarrier_gemm_pipelines_gb300 import _binding as b
     lib = b.lib()
-    M, N, K = 128, 2048, 2052          # K * N > 4194304
-    A = torch.zeros((M, K), device="cuda")
-    B = torch.zeros((K, N), device="cuda")
-    bias = torch.zeros(N, device="cuda")
-    C = torch.zeros((M, N), device="cuda")
+    M, N, K = 136, 2048, 2052
+    A, B, bias = inputs.gemm_normal(M, N, K, seed=25)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    assert _noalloc(lib, A.cuda(), B.cuda(), bias.cuda(), C, 4) == b.OK, b.last_error()
+    gbr.check_device()
+    _check_oracle(C, A, B, bias)
     before = lib.gbr_launch_count()
-    assert _noalloc(lib, A, B, bias, C, 3) == b.ERR_INVALID
-    assert "16 MiB" in b.last_error()
+    stream = torch.cuda.current_stream().cuda_stream
+    assert lib.gemm_bias_relu_tf32_noalloc(C.data_ptr(), C.data_ptr(), C.data_ptr(), C.data_ptr(),
+                                           1 << 31, 4, 4, 3, stream) == b.ERR_INVALID
+    assert "2^31" in b.last_error()
     assert lib.gbr_launch_count() == before
 
 
