@@ -227,6 +227,14 @@ int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage);
  *         such launches stay deterministic bit for bit (bf16 8192^3 on a
  *         152-SM GB300 does not split; TF32 4096^3 does).
  *         0: never, 1: whenever some tile can be split.
+ * GBR_F32_FFMA follows the same mode with its own combine: the whole tiles run
+ * in one launch, then the split tail's runs in a second launch of the same
+ * ring; each part of a split tile is stored in its own fp32 slot (sk tiles x
+ * 4 x 128 x 128 x 4 bytes), and the last CTA to finish a part adds the parts
+ * in part order, so FFMA results are the same bits on every call (they differ
+ * from the unsplit kernel's in the order of fp32 additions).  Its auto rule
+ * splits from a predicted saving of 1/50 (2%) of the launch (fp32 4096^3 on
+ * 152 SMs splits).  GBR_F32_FFMA_CPASYNC and GBR_F32_FFMA_SYNC never split.
  * GBR_ERR_INVALID for other values.  The failure-detection self tests and
  * gemm_bias_relu_tf32_noalloc never split.
  */

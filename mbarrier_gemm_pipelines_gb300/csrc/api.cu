@@ -311,13 +311,14 @@ int choose_pair(int64_t rows, int stages, int smem_optin, int* pair) {
 
 // Fills the split fields of `s` (see split_plan.cuh); returns the scratch
 // bytes the launch needs (0: no split).
-size_t plan_split(GemmShape& s, int64_t units, SplitScratch kind) {
+size_t plan_split(GemmShape& s, int64_t units, SplitScratch kind,
+                  int64_t gain_div = kSplitMinGainDiv) {
     int mode;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         mode = g_gemm_split;
     }
-    return plan_split_fields(s, units, mode) ? split_scratch_bytes(s, kind) : 0;
+    return plan_split_fields(s, units, mode, gain_div) ? split_scratch_bytes(s, kind) : 0;
 }
 
 // Dynamic tile order (the split tail is then off): requested, and usable?
@@ -342,14 +343,15 @@ int dynamic_scratch(const DevCtx& c, GemmShape& s, cudaStream_t st, void** ws) {
 }
 
 // Scratch of one split launch from the device's pool, zeroed on the stream:
-// the counters, then the tiles' sums.
+// the counters, then the tiles' sums (zero_sums false: the counters only).
 int split_scratch(const DevCtx& c, GemmShape& s, SplitScratch kind, size_t bytes, cudaStream_t st,
-                  void** ws) {
+                  void** ws, bool zero_sums = true) {
     *ws = nullptr;
     if (bytes == 0) return GBR_OK;
     cudaError_t e = cudaMallocFromPoolAsync(ws, bytes, c.pool, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync(split-tile scratch)");
-    if ((e = cudaMemsetAsync(*ws, 0, bytes, st)) != cudaSuccess) {
+    if ((e = cudaMemsetAsync(*ws, 0, zero_sums ? bytes : split_count_bytes(s, kind), st)) !=
+        cudaSuccess) {
         cudaFreeAsync(*ws, st);
         *ws = nullptr;
         return cuda_fail(e, "cudaMemsetAsync(split-tile scratch)");
@@ -780,7 +782,33 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
         });
         if (r != GBR_OK) return r;
         if (occ < 1) return fail(GBR_ERR_SMEM, "FFMA GEMM does not fit on an SM");
-        const int grid = int(std::min<int64_t>(s.num_tiles, int64_t(c->sm_count) * occ));
+        const int64_t units = int64_t(c->sm_count) * occ;
+        // The split tail (TMA producer): the whole tiles of the first rounds in
+        // one launch, then the last partial round's k-blocks dealt out evenly
+        // to every CTA in a second launch of the split instance.
+        GemmShape tail = s;
+        const size_t split_bytes =
+            dtype == GBR_F32_FFMA
+                ? plan_split(tail, units, ffma_split_scratch(), kSplitMinGainDivOrdered)
+                : 0;
+        if (split_bytes) {
+            void* ws = nullptr;
+            if ((r = split_scratch(*c, tail, ffma_split_scratch(), split_bytes, st, &ws, false)) !=
+                GBR_OK)
+                return r;
+            GemmShape whole = s;
+            whole.num_tiles = tail.dp_tiles;
+            e = launch_gemm_ffma(ma, mb, whole, int(units), smem, st, false, false);
+            if (e == cudaSuccess) {
+                ++g_launches;
+                e = launch_gemm_ffma(ma, mb, tail, int(units), smem, st, false, true);
+            }
+            cudaFreeAsync(ws, st);
+            if (e != cudaSuccess) return cuda_fail(e, "launching FFMA GEMM");
+            ++g_launches;
+            return GBR_OK;
+        }
+        const int grid = int(std::min<int64_t>(s.num_tiles, units));
         if ((e = launch_gemm_ffma(ma, mb, s, grid, smem, st, dtype == GBR_F32_FFMA_CPASYNC)) !=
             cudaSuccess)
             return cuda_fail(e, "launching FFMA GEMM");

@@ -112,10 +112,12 @@ size_t ffma_smem_bytes(int stages);
 cudaError_t ffma_prepare(size_t smem);
 cudaError_t ffma_occupancy(size_t smem, int* blocks_per_sm);
 cudaError_t ffma_check_registers(int* regs);
+// split: the launch runs the split tail of s (TMA producer only).
 cudaError_t launch_gemm_ffma(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmShape& s,
-                             int grid, size_t smem, cudaStream_t stream, bool cpasync = false);
+                             int grid, size_t smem, cudaStream_t stream, bool cpasync = false,
+                             bool split = false);
 // Consumer warps of the FFMA kernels (and of the homogeneous baseline's
-// micro-tile layout): 16 (default) or 8; returns 0, or -1 for other values.
+// micro-tile layout): 8 (default) or 16; returns 0, or -1 for other values.
 int ffma_set_consumer_warps(int cw);
 int ffma_consumer_warps();
 // Homogeneous baseline (every thread loads, syncs, computes, syncs); one CTA

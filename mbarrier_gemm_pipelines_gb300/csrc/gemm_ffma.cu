@@ -26,6 +26,7 @@
 // Slot/parity of k-iteration i (running across this CTA's tiles):
 //   slot = i % S, full parity = (i / S) & 1, empty parity = ((i / S) & 1) ^ 1.
 #include "gbr_internal.h"
+#include "split_plan.cuh"
 
 namespace gbr {
 
@@ -162,13 +163,85 @@ __device__ __forceinline__ void ffma_epilogue(const uint64_t (&acc)[8][NP], cons
     }
 }
 
+// Item j of this CTA: the whole tile blockIdx.x + j * gridDim.x of
+// [0, num_tiles), or (SPLIT) the CTA's run of k-blocks of the split tail,
+// which meets at most two tiles (the schedule of split_plan.cuh; the whole
+// tiles before it run in a separate launch).
+template <bool SPLIT>
+__device__ __forceinline__ bool ffma_item(const GemmShape& p, uint32_t j, WorkItem& w) {
+    if (!SPLIT) {
+        w.tile = blockIdx.x + j * gridDim.x;
+        w.kb0 = 0;
+        w.kb1 = p.num_kb;
+        w.part = 0;
+        w.parts = 1;
+        w.sk = 0;
+        return w.tile < uint32_t(p.num_tiles);
+    }
+    return work_item(p, blockIdx.x, gridDim.x, j + uint32_t(p.dp_tiles) / gridDim.x, w);
+}
+
+// Tile w.tile is split along K among w.parts CTAs.  Each stores its fp32 part
+// in its own 128 x 128 slot; the last CTA to finish its part adds the parts in
+// part order (so the result does not depend on which CTA arrives last), then
+// applies bias and ReLU.  No CTA waits for another.
+template <int CW, int NP>
+__device__ __forceinline__ void ffma_split_epilogue(const uint64_t (&acc)[8][NP],
+                                                    const GemmShape& p, const WorkItem& w,
+                                                    uint32_t mt, uint32_t nt, uint32_t tx,
+                                                    uint32_t ty, uint32_t ct,
+                                                    volatile int* last_flag) {
+    constexpr uint32_t kSlot = kFfmaBM * kFfmaBN;
+    float* slots = p.sk_sum + size_t(w.sk) * size_t(kSplitMaxParts) * kSlot;
+    float* mine = slots + size_t(w.part) * kSlot;
+#pragma unroll
+    for (int h = 0; h < NP / 2; ++h)
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const uint64_t lo = acc[r][2 * h], hi = acc[r][2 * h + 1];
+            __stcg(reinterpret_cast<float4*>(mine + (ty + 16u * r) * kFfmaBN + 4u * tx + 64u * h),
+                   make_float4(__uint_as_float(uint32_t(lo)), __uint_as_float(uint32_t(lo >> 32)),
+                               __uint_as_float(uint32_t(hi)), __uint_as_float(uint32_t(hi >> 32))));
+        }
+    __threadfence();
+    ptx::named_barrier_sync(1, Cons<CW>::threads);
+    if (ct == 0) {
+        const uint32_t arrived = atomicAdd(p.sk_count + w.sk, 1u) + 1u;
+        *last_flag = arrived == uint32_t(w.parts) ? 1 : 0;
+        __threadfence();
+    }
+    ptx::named_barrier_sync(1, Cons<CW>::threads);
+    if (!*last_flag) return;
+    uint64_t sum[8][NP];
+#pragma unroll
+    for (int h = 0; h < NP / 2; ++h)
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const size_t off = (ty + 16u * r) * kFfmaBN + 4u * tx + 64u * h;
+            float4 t = __ldcg(reinterpret_cast<const float4*>(slots + off));
+            for (int q = 1; q < w.parts; ++q) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(slots + q * kSlot + off));
+                t.x += v.x;
+                t.y += v.y;
+                t.z += v.z;
+                t.w += v.w;
+            }
+            sum[r][2 * h] = uint64_t(__float_as_uint(t.x)) | (uint64_t(__float_as_uint(t.y)) << 32);
+            sum[r][2 * h + 1] = uint64_t(__float_as_uint(t.z)) | (uint64_t(__float_as_uint(t.w)) << 32);
+        }
+    ffma_epilogue(sum, p, mt, nt, tx, ty);
+}
+
 // CPASYNC = false: one TMA lane produces each stage (the default).
 // CPASYNC = true: the historical producer ("gpu_warp_specialization" and
 // "pwwt.cn news/4436243" section 2: Ampere cp.async): the whole producer
 // warpgroup copies the stage with 16-byte cp.async per thread into the same
 // swizzled layout, and each of its 128 threads arrives on full[s] with
 // cp.async.mbarrier.arrive.noinc once its own copies have landed.
-template <int CW, bool CPASYNC>
+// SPLIT (TMA producer only): the launch runs the split tail of the schedule
+// instead of whole tiles; a separate instance, so that the whole-tile kernel
+// keeps its register allocation.
+template <int CW, bool CPASYNC, bool SPLIT = false>
 __global__ void __launch_bounds__(kThreads<CW>, 1)
     gemm_ffma_kernel(const __grid_constant__ CUtensorMap mapA,
                      const __grid_constant__ CUtensorMap mapB, const GemmShape p) {
@@ -179,6 +252,7 @@ __global__ void __launch_bounds__(kThreads<CW>, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + size_t(S) * kFfmaStageBytes);
     uint64_t* empty = full + S;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
+    volatile int* split_last = abort_flag + 1;   // SPLIT: this CTA finished its tile last
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     if (threadIdx.x == 0) {
@@ -209,11 +283,12 @@ __global__ void __launch_bounds__(kThreads<CW>, 1)
             const float* B = static_cast<const float*>(p.B);
             uint32_t i = 0, ntr = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            WorkItem w;
+            for (uint32_t j = 0; ok && ffma_item<SPLIT>(p, j, w); ++j) {
                 uint32_t mt, nt;
-                raster_tile(t, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+                raster_tile(w.tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
                 const int m0 = int(mt) * kFfmaBM, n0 = int(nt) * kFfmaBN;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++i) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++i) {
                     const uint32_t s = i % S, ph = (i / S) & 1u;
                     if (!mbar_wait_warp(ptx::smem_addr(empty + s), ph ^ 1u, p.ctl, abort_flag,
                                         kSiteProducerEmpty, i)) {
@@ -253,10 +328,11 @@ __global__ void __launch_bounds__(kThreads<CW>, 1)
             // ------------------------------------------------ producer
             uint32_t i = 0, ntr = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            WorkItem w;
+            for (uint32_t j = 0; ok && ffma_item<SPLIT>(p, j, w); ++j) {
                 uint32_t mt, nt;
-                raster_tile(t, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
-                for (int kb = 0; kb < p.num_kb; ++kb, ++i) {
+                raster_tile(w.tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++i) {
                     const uint32_t s = i % S, ph = (i / S) & 1u;
                     if (!mbar_wait(ptx::smem_addr(empty + s), ph ^ 1u, p.ctl, abort_flag,
                                    kSiteProducerEmpty, i)) {
@@ -299,13 +375,14 @@ __global__ void __launch_bounds__(kThreads<CW>, 1)
         uint32_t i = 0, ntr = 0;
         const bool tracer = p.ctl.trace != nullptr && warp == 4 && lane == 0;   // one consumer lane
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        WorkItem w;
+        for (uint32_t j = 0; ok && ffma_item<SPLIT>(p, j, w); ++j) {
             uint32_t mt, nt;
-            raster_tile(t, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+            raster_tile(w.tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
             uint64_t acc[8][L::np];
             ffma_zero(acc);
 
-            for (int kb = 0; kb < p.num_kb; ++kb, ++i) {
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++i) {
                 const uint32_t s = i % S, ph = (i / S) & 1u;
                 if (!mbar_wait_warp(ptx::smem_addr(full + s), ph, p.ctl, abort_flag,
                                     kSiteConsumerFull, i)) {
@@ -321,7 +398,10 @@ __global__ void __launch_bounds__(kThreads<CW>, 1)
             }
             if (!ok) break;
 
-            ffma_epilogue(acc, p, mt, nt, tx, ty);
+            if (SPLIT)
+                ffma_split_epilogue<CW>(acc, p, w, mt, nt, tx, ty, ct, split_last);
+            else
+                ffma_epilogue(acc, p, mt, nt, tx, ty);
         }
         if (tracer) trace_count(p.ctl, kRoleConsumer, ntr);
     }
@@ -407,7 +487,8 @@ int ffma_warps_now() {
 }
 
 template <int CW>
-const void* ffma_fn(bool cpasync) {
+const void* ffma_fn(bool cpasync, bool split = false) {
+    if (split) return reinterpret_cast<const void*>(gemm_ffma_kernel<CW, false, true>);
     return cpasync ? reinterpret_cast<const void*>(gemm_ffma_kernel<CW, true>)
                    : reinterpret_cast<const void*>(gemm_ffma_kernel<CW, false>);
 }
@@ -433,20 +514,20 @@ cudaError_t launch_gemm_ffma_sync(const float* A, const float* B, const GemmShap
 }
 
 size_t ffma_smem_bytes(int stages) {
-    return 1024 + size_t(stages) * kFfmaStageBytes + size_t(2 * stages) * 8 + 16;
+    return 1024 + size_t(stages) * kFfmaStageBytes + size_t(2 * stages) * 8 + 16;   // + flags
 }
 
 cudaError_t ffma_prepare(size_t smem) {
     static std::mutex mu;
-    static size_t set[kMaxDeviceSlots][4] = {};
+    static size_t set[kMaxDeviceSlots][6] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDeviceSlots) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(mu);
-    const void* fns[4] = {ffma_fn<8>(false), ffma_fn<8>(true), ffma_fn<16>(false),
-                          ffma_fn<16>(true)};
-    for (int i = 0; i < 4; ++i)
+    const void* fns[6] = {ffma_fn<8>(false), ffma_fn<8>(true), ffma_fn<16>(false),
+                          ffma_fn<16>(true), ffma_fn<8>(false, true), ffma_fn<16>(false, true)};
+    for (int i = 0; i < 6; ++i)
         if ((e = raise_smem_limit(fns[i], smem, &set[dev][i])) != cudaSuccess) return e;
     return cudaSuccess;
 }
@@ -464,7 +545,7 @@ cudaError_t ffma_occupancy(size_t smem, int* blocks_per_sm) {
 template <int CW>
 cudaError_t ffma_check_registers_cw(int* regs) {
     const long need = 128L * Cons<CW>::producer_regs + long(Cons<CW>::threads) * Cons<CW>::regs;
-    for (const void* fn : {ffma_fn<CW>(false), ffma_fn<CW>(true)}) {
+    for (const void* fn : {ffma_fn<CW>(false), ffma_fn<CW>(true), ffma_fn<CW>(false, true)}) {
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, fn);
         if (e != cudaSuccess) return e;
@@ -481,7 +562,7 @@ cudaError_t ffma_check_registers(int* regs) {
 }
 
 cudaError_t launch_gemm_ffma(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmShape& s,
-                             int grid, size_t smem, cudaStream_t stream, bool cpasync) {
+                             int grid, size_t smem, cudaStream_t stream, bool cpasync, bool split) {
     const int cw = ffma_warps_now();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));
@@ -491,6 +572,10 @@ cudaError_t launch_gemm_ffma(const CUtensorMap& mapA, const CUtensorMap& mapB, c
     cudaLaunchAttribute attr[1];
     cfg.numAttrs = programmatic_launch_attr(attr);
     cfg.attrs = attr;
+    if (split) {
+        if (cw == 16) return cudaLaunchKernelEx(&cfg, gemm_ffma_kernel<16, false, true>, mapA, mapB, s);
+        return cudaLaunchKernelEx(&cfg, gemm_ffma_kernel<8, false, true>, mapA, mapB, s);
+    }
     if (cw == 16) {
         if (cpasync) return cudaLaunchKernelEx(&cfg, gemm_ffma_kernel<16, true>, mapA, mapB, s);
         return cudaLaunchKernelEx(&cfg, gemm_ffma_kernel<16, false>, mapA, mapB, s);

@@ -88,7 +88,8 @@ inline int64_t split_cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // k-blocks, so that small problems keep their single launch, and by at least
 // 1/kSplitMinGainDiv of the whole launch; 1: whenever a tile can be split;
 // 0: never).  Returns true when the launch splits.
-inline bool plan_split_fields(GemmShape& s, int64_t units, int mode) {
+inline bool plan_split_fields(GemmShape& s, int64_t units, int mode,
+                              int64_t gain_div = kSplitMinGainDiv) {
     s.dp_tiles = s.sk_tiles = s.sk_iters = 0;
     s.sk_sum = nullptr;
     s.sk_count = nullptr;
@@ -103,7 +104,7 @@ inline bool plan_split_fields(GemmShape& s, int64_t units, int mode) {
     if (run < run_min) run = run_min;
     if (run >= nkb) return false;
     if (mode < 0 && (run * 8 > nkb * 7 || nkb - run < kSplitMinSaving ||
-                     (nkb - run) * kSplitMinGainDiv < split_cdiv(T, units) * nkb))
+                     (nkb - run) * gain_div < split_cdiv(T, units) * nkb))
         return false;
     s.dp_tiles = int32_t(T - R);
     s.sk_tiles = int32_t(R);
@@ -128,6 +129,15 @@ inline size_t split_scratch_bytes(const GemmShape& s, SplitScratch k) {
 // tcgen05 kernel: per CTA of the tile, 4 epilogue warps; 128 rows per CTA x 256.
 inline SplitScratch umma_split_scratch(int pair) {
     return SplitScratch{size_t(pair) * 4u * 2u, size_t(kUmmaBM * pair) * size_t(kUmmaBN)};
+}
+// FFMA kernel: one arrival count per split tile, and one 128 x 128 fp32 slot
+// per part (each part writes its own slot whole, so only the counts are
+// zeroed).  Its parts are added in a fixed order, so a split launch is
+// deterministic bit for bit, and auto splits from a predicted saving of
+// 1/kSplitMinGainDivOrdered of the launch.
+constexpr int64_t kSplitMinGainDivOrdered = 50;
+inline SplitScratch ffma_split_scratch() {
+    return SplitScratch{1u, size_t(kSplitMaxParts) * size_t(kFfmaBM) * size_t(kFfmaBN)};
 }
 
 }  // namespace gbr

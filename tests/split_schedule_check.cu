@@ -29,12 +29,14 @@ int main() {
     for (int units : unit_list)
         for (int T : tile_list)
             for (int nkb : kb_list)
-                for (int mode : {-1, 0, 1}) {
+                for (int mode_gd = 0; mode_gd < 6; ++mode_gd) {
+                    const int mode = mode_gd % 3 - 1;
+                    const int64_t gain_div = mode_gd < 3 ? kSplitMinGainDiv : kSplitMinGainDivOrdered;
                     GemmShape s;
                     std::memset(&s, 0, sizeof(s));
                     s.num_tiles = T;
                     s.num_kb = nkb;
-                    const bool split = plan_split_fields(s, units, mode);
+                    const bool split = plan_split_fields(s, units, mode, gain_div);
                     ++configs;
                     split_configs += split;
                     if (split != (s.sk_tiles > 0)) return fail("plan flag", units, T, nkb, mode);
@@ -87,6 +89,21 @@ int main() {
                     if (split && longest_split_run >= nkb)
                         return fail("split round not shorter than a tile", units, T, nkb, mode);
                 }
+    // The two auto rules on the workloads they were set for: fp32 4096^3 FFMA
+    // (1024 tiles of 128 x 32 k-blocks on 152 CTAs) splits under the ordered
+    // rule only; bf16 8192^3 on 76 CTA pairs (1024 tiles, 64 k-blocks of 128)
+    // does not split under the tensor-core kernels' 5% rule.
+    {
+        GemmShape s;
+        std::memset(&s, 0, sizeof(s));
+        s.num_tiles = 1024;
+        s.num_kb = 128;
+        if (plan_split_fields(s, 152, -1)) return fail("ffma 4096 auto, 5% rule", 152, 1024, 128, -1);
+        if (!plan_split_fields(s, 152, -1, kSplitMinGainDivOrdered))
+            return fail("ffma 4096 auto, ordered rule", 152, 1024, 128, -1);
+        s.num_kb = 64;
+        if (plan_split_fields(s, 76, -1)) return fail("bf16 8192 auto", 76, 1024, 64, -1);
+    }
     std::printf("ok %ld configurations, %ld split\n", configs, split_configs);
     return 0;
 }

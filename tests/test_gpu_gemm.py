@@ -152,7 +152,8 @@ SPLIT_SHAPES = [(383, 776, 1352), (520, 264, 4096), (130, 2056, 3000), (2304, 23
                 (256, 256, 8192)]
 
 
-@pytest.mark.parametrize("dtype,pair", [("tf32", 1), ("tf32", 2), ("bf16", 1), ("bf16", 2)])
+@pytest.mark.parametrize("dtype,pair", [("tf32", 1), ("tf32", 2), ("bf16", 1), ("bf16", 2),
+                                        ("ffma", -1)])
 @pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
 def test_split_tail(gbr, dtype, pair, M, N, K):
     """Last round split along K (forced on): parity with the oracle element by
@@ -167,6 +168,20 @@ def test_split_tail(gbr, dtype, pair, M, N, K):
             whole = _run(gbr, A, B, bias, dtype, 3)
     _check_full(got, A.float(), B.float(), bias, dtype)
     assert rel_frobenius(got, whole) <= TOL[dtype] / 10
+
+
+@pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
+def test_ffma_split_tail_is_ordered(gbr, M, N, K):
+    """The FFMA split tail (whole tiles in one launch, the last round's
+    k-blocks dealt to every CTA in a second) adds each tile's parts in part
+    order: the same bits on every call and with either consumer layout."""
+    A, B, bias = inputs.gemm_normal(M, N, K, seed=M * 3 + N + K)
+    outs = []
+    with split_tail(gbr, 1):
+        for warps in (8, 8, 16):
+            with ffma_warps(gbr, warps):
+                outs.append(_run(gbr, A, B, bias, "ffma", 3))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
 
 
 def test_split_tail_mode_is_validated(gbr):
@@ -326,6 +341,16 @@ def test_config4_bf16_8192(gbr, bf16_8192, S, pair, ks):
     element against the oracle."""
     with tuned(gbr, pair, ks):
         _full_size(gbr, bf16_8192, "bf16", S)
+
+
+def test_config3_ffma_default_is_deterministic(gbr, fp32_4096):
+    """fp32 4096^3 FFMA at S = 3, the default (the split tail is on: 1024
+    tiles on 152 CTAs): two calls in a row give the same bits."""
+    A, B, bias = (t.cuda() for t in fp32_4096[:3])
+    C1 = gbr.gemm_bias_relu(A, B, bias, dtype="ffma", stages=3)
+    C2 = gbr.gemm_bias_relu(A, B, bias, dtype="ffma", stages=3)
+    gbr.check_device()
+    assert torch.equal(C1, C2)
 
 
 def test_config4_default_is_deterministic(gbr, bf16_8192):
