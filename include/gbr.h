@@ -234,7 +234,9 @@ int gbr_gemm_tuning(int cta_pair, int group_m, int l2_hint, int k_per_stage);
  * in part order, so FFMA results are the same bits on every call (they differ
  * from the unsplit kernel's in the order of fp32 additions).  Its auto rule
  * splits from a predicted saving of 1/50 (2%) of the launch (fp32 4096^3 on
- * 152 SMs splits).  GBR_F32_FFMA_CPASYNC and GBR_F32_FFMA_SYNC never split.
+ * 152 SMs splits).  GBR_F32_FFMA_CPASYNC and GBR_F32_FFMA_SYNC never split,
+ * and GBR_F32_FFMA does not while gbr_trace_buffer is set (its two launches
+ * would each write the trace from the start).
  * GBR_ERR_INVALID for other values.  The failure-detection self tests and
  * gemm_bias_relu_tf32_noalloc never split.
  */

@@ -785,10 +785,12 @@ int gemm_bias_relu(const void* A, const void* B, const float* bias, void* C, int
         const int64_t units = int64_t(c->sm_count) * occ;
         // The split tail (TMA producer): the whole tiles of the first rounds in
         // one launch, then the last partial round's k-blocks dealt out evenly
-        // to every CTA in a second launch of the split instance.
+        // to every CTA in a second launch of the split instance.  Not while an
+        // event trace is recorded: each launch writes its CTAs' trace from the
+        // start, so the second would overwrite the first.
         GemmShape tail = s;
         const size_t split_bytes =
-            dtype == GBR_F32_FFMA
+            dtype == GBR_F32_FFMA && s.ctl.trace == nullptr
                 ? plan_split(tail, units, ffma_split_scratch(), kSplitMinGainDivOrdered)
                 : 0;
         if (split_bytes) {

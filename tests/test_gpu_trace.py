@@ -83,6 +83,24 @@ def test_ffma_trace(gbr, dtype, S):
     assert replay_units(ev, S) >= 16
 
 
+def test_ffma_trace_keeps_one_launch(gbr):
+    """With the split tail forced on, an FFMA call under the event trace still
+    runs as one launch (a split call's second launch would overwrite the first
+    one's trace): 256 tiles x 32 k-blocks, every ring item consumed once in
+    the record."""
+    A, B, bias = inputs.gemm_normal(2048, 2048, 1024, seed=32)
+    with split_tail(gbr, 1):
+        with trace.Recorder(cap=256) as rec:
+            C = gbr.gemm_bias_relu(A.cuda(), B.cuda(), bias.cuda(), dtype="ffma", stages=3)
+            ev, cnt = rec.events()
+    gbr.check_device()
+    assert rel_frobenius(to_host_f64(C), oracle.gemm_bias_relu(A, B, bias)) <= TOL["ffma"]
+    assert check(ev, cnt, 3) == []
+    released = sum(int((r["ev"] == trace.RELEASED).sum()) for (cta, role), r in ev.items()
+                   if role == roles.CONSUMER)
+    assert released == 256 * 32
+
+
 @pytest.mark.parametrize("dtype,pair,ks,S,split", [
     ("bf16", 2, 2, 3, -1), ("bf16", 2, 1, 6, 0), ("bf16", 1, 1, 4, -1), ("bf16", 1, 2, 2, 1),
     ("tf32", 2, 2, 3, 1), ("tf32", 1, 1, 3, 0),
