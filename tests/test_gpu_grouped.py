@@ -62,11 +62,12 @@ def test_grouped_matches_dense_per_expert(gbr, pair):
 def test_grouped_split_tail(gbr, pair):
     """The last round split along K (forced on), tiles of several experts among
     the split ones: parity with the oracle, and the unsplit result up to the
-    order of fp32 additions."""
+    order of fp32 additions.  (Thin tail tiles turn the split off, so they are
+    off here.)"""
     counts = [300, 0, 513, 77, 1]
     cnt, X, W, b = inputs.grouped(tokens=sum(counts), experts=5, K=1024, N=1032, seed=21)
     dX, dW, db = X.cuda(), W.cuda(), b.cuda()
-    with tuned(gbr, pair):
+    with tuned(gbr, pair), thin_tail(gbr, False):
         with split_tail(gbr, 1):
             C = gbr.gemm_bias_relu_grouped(dX, dW, db, counts, stages=3)
         with split_tail(gbr, 0):
