@@ -193,8 +193,8 @@ int gbr_copy_tuning(int store_lag, int ctas_per_sm, int l2_hint);
  * GBR_F32_TF32, and gemm_bias_relu_grouped).  cta_pair: -1 auto, 1 (one CTA
  * per 128x256 output tile, S <= 4), 2 (a two-CTA cluster per 256x256 tile,
  * cta_group::2 MMA, S <= 6).  Auto picks 2 when there is more than one
- * 128-row tile or S > 4 (grouped: when 256-row tiles waste at most ~10% more
- * rows).  group_m: -1 auto, else output-tile rows per raster band.
+ * 128-row tile or S > 4 (grouped: when some expert has more than 128 rows, or
+ * S > 4).  group_m: -1 auto, else output-tile rows per raster band.
  * l2_hint: L2 eviction priority of the A/B tile loads: -1 auto (none), 0 none,
  * 1 both evict_last, 2 A evict_first + B evict_last, 3 A evict_last + B
  * evict_first, 4 both evict_normal.  k_per_stage: 1 or 2 slices of 128 bytes

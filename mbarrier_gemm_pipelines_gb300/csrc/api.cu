@@ -946,14 +946,14 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
     s.k_sub = uint32_t(k_sub_forced() == 2 ? 2 : 1);
     int pair = 1;
     {
-        // Auto: the pair when its 256-row tiles waste at most ~10% more rows
-        // than 128-row tiles over the experts' row counts.
-        int64_t rows1 = 0, rows2 = 0, maxn = 0;
-        for (int e2 = 0; e2 < num_groups; ++e2) {
-            rows1 += cdiv(counts_host[e2], 128) * 128;
-            rows2 += cdiv(counts_host[e2], 256) * 256;
-            maxn = std::max<int64_t>(maxn, counts_host[e2]);
-        }
+        // Auto: the pair as soon as some expert spans more than one 128-row
+        // tile.  Measured on GB300 (K 4096, N 14336), a 128 x 256 one-CTA tile
+        // costs about 0.65 of a 256 x 256 pair tile, so the pair is cheaper
+        // even where its 256-row tiles pad more rows (skewed experts of 2048
+        // down to 32 rows: 1465 against 1107 TFLOP/s); the short tails run as
+        // thin tiles.
+        int64_t maxn = 0;
+        for (int e2 = 0; e2 < num_groups; ++e2) maxn = std::max<int64_t>(maxn, counts_host[e2]);
         int forced;
         {
             std::lock_guard<std::mutex> lk(g_mu);
@@ -966,7 +966,7 @@ int gemm_bias_relu_grouped(const void* X, const void* W, const float* bias, void
         if (forced > 0)
             pair = forced;
         else
-            pair = (stages > max1 || (maxn > 128 && rows2 * 10 <= rows1 * 11)) ? 2 : 1;
+            pair = (stages > max1 || maxn > 128) ? 2 : 1;
         if (pair == 2 && stages > max2)
             return fail(GBR_ERR_SMEM, "stages=%d exceeds %d for this stage size", stages, max2);
         s.k_sub = uint32_t(choose_k_sub(pair, stages, c->smem_optin));
