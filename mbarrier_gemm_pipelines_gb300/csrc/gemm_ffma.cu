@@ -181,16 +181,18 @@ __device__ __forceinline__ bool ffma_item(const GemmShape& p, uint32_t j, WorkIt
     return work_item(p, blockIdx.x, gridDim.x, j + uint32_t(p.dp_tiles) / gridDim.x, w);
 }
 
-// Tile w.tile is split along K among w.parts CTAs.  Each stores its fp32 part
-// in its own 128 x 128 slot; the last CTA to finish its part adds the parts in
-// part order (so the result does not depend on which CTA arrives last), then
-// applies bias and ReLU.  No CTA waits for another.
+// Tile w.tile is split along K among w.parts CTAs.  Each CTA stores its fp32
+// part in its own 128 x 128 slot.  Every consumer warp owns a fixed set of the
+// tile's elements in every CTA and counts its arrival on its own counter; the
+// warp whose arrival completes a count adds that warp region's parts in part
+// order (so the result does not depend on which CTA arrives last), then
+// applies bias and ReLU.  No warp waits for another warp or CTA, so a warp
+// that left its loop after a timeout cannot hold up the rest.
 template <int CW, int NP>
 __device__ __forceinline__ void ffma_split_epilogue(const uint64_t (&acc)[8][NP],
                                                     const GemmShape& p, const WorkItem& w,
                                                     uint32_t mt, uint32_t nt, uint32_t tx,
-                                                    uint32_t ty, uint32_t ct,
-                                                    volatile int* last_flag) {
+                                                    uint32_t ty, uint32_t ct) {
     constexpr uint32_t kSlot = kFfmaBM * kFfmaBN;
     float* slots = p.sk_sum + size_t(w.sk) * size_t(kSplitMaxParts) * kSlot;
     float* mine = slots + size_t(w.part) * kSlot;
@@ -204,14 +206,13 @@ __device__ __forceinline__ void ffma_split_epilogue(const uint64_t (&acc)[8][NP]
                                __uint_as_float(uint32_t(hi)), __uint_as_float(uint32_t(hi >> 32))));
         }
     __threadfence();
-    ptx::named_barrier_sync(1, Cons<CW>::threads);
-    if (ct == 0) {
-        const uint32_t arrived = atomicAdd(p.sk_count + w.sk, 1u) + 1u;
-        *last_flag = arrived == uint32_t(w.parts) ? 1 : 0;
-        __threadfence();
-    }
-    ptx::named_barrier_sync(1, Cons<CW>::threads);
-    if (!*last_flag) return;
+    __syncwarp();
+    uint32_t arrived = 0;
+    if ((ct & 31u) == 0)
+        arrived = atomicAdd(p.sk_count + size_t(w.sk) * kFfmaMaxConsumerWarps + (ct >> 5), 1u) + 1u;
+    arrived = __shfl_sync(0xffffffffu, arrived, 0);
+    if (arrived != uint32_t(w.parts)) return;
+    __threadfence();
     uint64_t sum[8][NP];
 #pragma unroll
     for (int h = 0; h < NP / 2; ++h)
@@ -252,7 +253,6 @@ __global__ void __launch_bounds__(kThreads<CW>, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + size_t(S) * kFfmaStageBytes);
     uint64_t* empty = full + S;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
-    volatile int* split_last = abort_flag + 1;   // SPLIT: this CTA finished its tile last
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     if (threadIdx.x == 0) {
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kThreads<CW>, 1)
             if (!ok) break;
 
             if (SPLIT)
-                ffma_split_epilogue<CW>(acc, p, w, mt, nt, tx, ty, ct, split_last);
+                ffma_split_epilogue<CW>(acc, p, w, mt, nt, tx, ty, ct);
             else
                 ffma_epilogue(acc, p, mt, nt, tx, ty);
         }

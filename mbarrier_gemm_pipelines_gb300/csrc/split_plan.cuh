@@ -130,14 +130,16 @@ inline size_t split_scratch_bytes(const GemmShape& s, SplitScratch k) {
 inline SplitScratch umma_split_scratch(int pair) {
     return SplitScratch{size_t(pair) * 4u * 2u, size_t(kUmmaBM * pair) * size_t(kUmmaBN)};
 }
-// FFMA kernel: one arrival count per split tile, and one 128 x 128 fp32 slot
-// per part (each part writes its own slot whole, so only the counts are
-// zeroed).  Its parts are added in a fixed order, so a split launch is
+// FFMA kernel: an arrival count per consumer warp per split tile, and one
+// 128 x 128 fp32 slot per part (each part writes its own slot whole, so only
+// the counts are zeroed).  Its parts are added in a fixed order, so a split launch is
 // deterministic bit for bit, and auto splits from a predicted saving of
 // 1/kSplitMinGainDivOrdered of the launch.
 constexpr int64_t kSplitMinGainDivOrdered = 50;
+constexpr uint32_t kFfmaMaxConsumerWarps = 16;
 inline SplitScratch ffma_split_scratch() {
-    return SplitScratch{1u, size_t(kSplitMaxParts) * size_t(kFfmaBM) * size_t(kFfmaBN)};
+    return SplitScratch{kFfmaMaxConsumerWarps,
+                        size_t(kSplitMaxParts) * size_t(kFfmaBM) * size_t(kFfmaBN)};
 }
 
 }  // namespace gbr
