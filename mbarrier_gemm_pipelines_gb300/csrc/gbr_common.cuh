@@ -25,6 +25,7 @@ enum WaitSite : uint32_t {
     kSiteEpiAccFull = 0x41,
     kSiteEpiSplitSum = 0x42,
     kSiteEpiTile = 0x43,
+    kSiteEpiBias = 0x44,
     kSiteStorerFull = 0x51,
     kSiteSelfTest = 0x71,
 };

@@ -134,6 +134,9 @@ constexpr uint32_t kUmmaEpiBytes = 4 * 2 * 32 * 128;        // 4 warps x 2 buffe
 // Barriers and small per-CTA words after the epilogue staging: 20 S + 132
 // bytes for S ring stages (S <= 6 on every kernel instance), rounded up.
 constexpr uint32_t kUmmaBarrierBytes = 384;
+// The tile's bias (256 fp32), staged in shared memory by a bulk copy for the
+// epilogue; after the barriers.
+constexpr uint32_t kUmmaBiasBytes = kUmmaBN * 4;
 constexpr int kMaxGroups = 32;
 
 // Operand types of the tensor-core GEMM; both read A K-major from A[M, K] and

@@ -56,7 +56,8 @@ cudaError_t launch_umma(int kind, int pair, const UmmaParams<GROUPED>& P, int gr
 
 size_t umma_ring_bytes(int stages, int pair, int k_sub) {
     const size_t stage = pair == 2 ? Pair<2>::stage_bytes : Pair<1>::stage_bytes;
-    return 1024 + size_t(stages) * size_t(k_sub) * stage + kUmmaEpiBytes + kUmmaBarrierBytes;
+    return 1024 + size_t(stages) * size_t(k_sub) * stage + kUmmaEpiBytes + kUmmaBarrierBytes +
+           kUmmaBiasBytes;
 }
 
 size_t umma_smem_bytes(int stages, int pair, int k_sub) {

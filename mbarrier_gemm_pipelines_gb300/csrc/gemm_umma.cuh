@@ -351,11 +351,11 @@ __device__ __forceinline__ void acc_release(uint32_t ae, uint32_t lane) {
 // given row the warp's lanes write 32 consecutive columns.  The accumulator
 // may be released once this returns (every tcgen05.ld has completed).
 __device__ __forceinline__ void thin_epilogue(const GemmShape& s, const TileInfo& ti,
-                                              const float* bias, int32_t group_row0,
+                                              const float* bias_sm, int32_t group_row0,
                                               uint32_t tcol, uint32_t col, bool zero_acc) {
     const int n = ti.n0 + int(col);
     const bool col_in = n < s.N;
-    const float bv = col_in ? __ldg(bias + n) : 0.f;
+    const float bv = col_in ? bias_sm[col] : 0.f;   // the tile's bias, staged in shared memory
     const size_t pitch = size_t(s.N);
     __nv_bfloat16* cp = static_cast<__nv_bfloat16*>(s.C) +
                         size_t(group_row0 + ti.c_row) * pitch + size_t(n);
@@ -483,6 +483,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tiles.empty = tiles.full + kTileRing;
     tiles.ids = reinterpret_cast<uint32_t*>(tiles.empty + kTileRing);
     uint32_t* issued_word = tiles.ids + kTileRing;   // ring items this CTA's producer issued
+    // The epilogue's bias slot: bias_full (one arrive.expect_tx + the bulk
+    // copy's bytes), bias_empty (the 4 epilogue warps of this CTA).
+    uint64_t* bias_full = reinterpret_cast<uint64_t*>(issued_word + 2);
+    uint64_t* bias_empty = bias_full + 1;
+    const float* bias_sm = reinterpret_cast<const float*>(epi + kUmmaEpiBytes + kUmmaBarrierBytes);
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const uint32_t rank = PAIR == 2 ? ptx::cluster_ctarank() : 0u;
@@ -499,6 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(ptx::smem_addr(acc_empty + a), 4 * PAIR);        // epilogue warps
         }
         ptx::mbar_init(ptx::smem_addr(drain), 1);
+        ptx::mbar_init(ptx::smem_addr(bias_full), 1);
+        ptx::mbar_init(ptx::smem_addr(bias_empty), 4);
         for (uint32_t d = 0; d < kTileRing; ++d) {
             ptx::mbar_init(ptx::smem_addr(tiles.full + d), 1);
             // readers: the MMA lane, the epilogue warps of the unit, the odd CTA's producer
@@ -678,6 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t row_off = lane * 128u;
         const uint32_t swz = lane & 7u;
         uint32_t chunk_ctr = 0, ntr = 0;
+        uint32_t bias_issued = 0;                     // warp 0: bias copies issued
         const bool tracer = kTrace && s.ctl.trace != nullptr && q == 0 && lane == 0;   // one lane
         const bool dyn = kDyn && s.dyn_counter != nullptr;
         WorkItem w;
@@ -688,6 +696,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const TileInfo ti = decode_tile<GROUPED, PAIR>(P, w.tile, rank);
             const uint32_t a = tl & 1u, aph = (tl >> 1) & 1u;
             const uint32_t ae = ptx::smem_addr(acc_empty + a);
+            // Warp 0 stages this item's bias (the tile's columns that lie
+            // inside N) once all 4 warps are done with the previous item's.
+            // The copy lands while the item's mainloop runs.
+            if (q == 0) {
+                if (tl > 0 && !mbar_wait_warp(ptx::smem_addr(bias_empty), (tl - 1u) & 1u, s.ctl,
+                                              abort_flag, kSiteEpiBias, tl))
+                    break;
+                if (lane == 0) {
+                    const int32_t cols = s.N - ti.n0 < int32_t(kUmmaBN) ? s.N - ti.n0 : int32_t(kUmmaBN);
+                    const uint32_t bytes = uint32_t(cols) * 4u;
+                    const uint32_t bf = ptx::smem_addr(bias_full);
+                    ptx::mbar_arrive_expect_tx(bf, bytes);
+                    ptx::bulk_load(ptx::smem_addr(bias_sm),
+                                   s.bias + (GROUPED ? P.bias_group_stride * ti.group : 0) + ti.n0,
+                                   bytes, bf);
+                }
+                ++bias_issued;
+            }
             if (!mbar_wait_warp<kCl>(ptx::smem_addr(acc_full + a), aph, s.ctl, abort_flag,
                                      kSiteEpiAccFull, tl))
                 break;
@@ -724,6 +750,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __threadfence();
                     __syncwarp();
                     if (lane == 0) atomicAdd(arrived + 1, 1u);
+                    // This part runs no epilogue, but hands the bias slot on.
+                    if (!mbar_wait_warp(ptx::smem_addr(bias_full), tl & 1u, s.ctl, abort_flag,
+                                        kSiteEpiBias, tl))
+                        break;
+                    if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(bias_empty));
                     continue;
                 }
                 bool ok = true;
@@ -734,16 +765,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __threadfence();
                 sum = blk;
             }
-            const float* bias = s.bias + (GROUPED ? P.bias_group_stride * ti.group : 0);
+            if (!mbar_wait_warp(ptx::smem_addr(bias_full), tl & 1u, s.ctl, abort_flag,
+                                kSiteEpiBias, tl))
+                break;
             if (GROUPED && PAIR == 2 && KIND == kUmmaBf16 && ti.thin > 0) {
                 // Thin tile: the accumulator holds C^T, TMEM lane = output
                 // column, column j = row j of the tile.  Each lane stores its
                 // column of the tile's rows; a warp's 32 lanes write 64
                 // contiguous bytes of a row.  (Thin tiles are never split.)
-                thin_epilogue(s, ti, bias, P.g.row_off[ti.group], tmem_base + lane_base + a * kAccCols,
-                              rank * 128u + q * 32u + lane, zero_acc);
+                thin_epilogue(s, ti, bias_sm, P.g.row_off[ti.group],
+                              tmem_base + lane_base + a * kAccCols, rank * 128u + q * 32u + lane,
+                              zero_acc);
                 if (tracer) trace_event(s.ctl, kRoleEpilogue, ntr, kEvReleased, tl, a, 0);
                 acc_release<PAIR>(ae, lane);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(bias_empty));
                 continue;
             }
             const CUtensorMap* mapC = &P.mapC[GROUPED ? ti.group : 0];
@@ -771,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j4 = 0; j4 < 8; ++j4) {
                             const int n = ti.n0 + int(col0) + 32 * h + 4 * j4;
                             float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (n < s.N) b = __ldg(reinterpret_cast<const float4*>(bias + n));
+                            if (n < s.N) b = *reinterpret_cast<const float4*>(bias_sm + (n - ti.n0));
                             const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
                             for (int u = 0; u < 2; ++u) {
@@ -797,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j4 = 0; j4 < 8; ++j4) {
                         const int n = ti.n0 + int(col0) + 4 * j4;
                         float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (n < s.N) b = __ldg(reinterpret_cast<const float4*>(bias + n));
+                        if (n < s.N) b = *reinterpret_cast<const float4*>(bias_sm + (n - ti.n0));
                         const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
@@ -823,7 +859,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::bulk_commit_group();
                 }
             }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(bias_empty));   // done with this bias
         }
+        // The last bias copy issued has landed before the CTA may exit (it
+        // has, unless an abort left its item unconsumed).
+        if (q == 0 && lane == 0 && bias_issued > 0)
+            mbar_wait_drain(ptx::smem_addr(bias_full), (bias_issued - 1u) & 1u, s.ctl.timeout_ns);
         if (tracer) trace_count(s.ctl, kRoleEpilogue, ntr);
         if (lane == 0) ptx::bulk_wait_group<0>();
     }

@@ -166,7 +166,8 @@ extern "C" int gemm_bias_relu_tf32_noalloc(const float* A, const float* B, const
     // One CTA per 128x256 tile: as many 48 KiB stages as fit beside the
     // epilogue staging (4 on GB300).
     int smax = 0;
-    while (smax < 16 && 1024 + size_t(smax + 1) * kUmmaStageBytes + kUmmaEpiBytes + kUmmaBarrierBytes <=
+    while (smax < 16 && 1024 + size_t(smax + 1) * kUmmaStageBytes + kUmmaEpiBytes + kUmmaBarrierBytes +
+                                kUmmaBiasBytes <=
                             size_t(d->smem_optin))
         ++smax;
     if (stages < 1 || stages > smax) {
