@@ -155,6 +155,29 @@ def test_grouped_trace(gbr, pair):
     assert replay_units(ev, 3, cta_group=pair, accumulator=True) >= 1
 
 
+@pytest.mark.parametrize("counts,pair", [([2048, 1024, 512, 256, 128, 64, 32, 32], 2),
+                                         ([100, 64, 128, 1], 1)])
+def test_grouped_auto_pair_choice(gbr, counts, pair):
+    """The automatic choice between one CTA and the CTA pair: the pair as soon
+    as an expert spans more than one 128-row tile (skewed experts included),
+    one CTA when every expert fits one.  Seen in the trace: a pair launch runs
+    its MMA lane on even CTAs only."""
+    cnt_, X, W, b = inputs.grouped(tokens=sum(counts), experts=len(counts), K=256, N=520,
+                                   seed=35)
+    with trace.Recorder(cap=1024) as rec:
+        C = gbr.gemm_bias_relu_grouped(X.cuda(), W.cuda(), b.cuda(), counts, stages=3)
+        ev, cnt = rec.events()
+    gbr.check_device()
+    ref = oracle.gemm_bias_relu_grouped(X.float(), W.float(), b, counts)
+    assert rel_frobenius(to_host_f64(C), ref) <= TOL["bf16"]
+    mma_ctas = {cta for (cta, role) in ev if role == roles.CONSUMER}
+    assert mma_ctas
+    if pair == 2:
+        assert all(c % 2 == 0 for c in mma_ctas)
+    else:
+        assert any(c % 2 == 1 for c in mma_ctas)
+
+
 def test_trace_off_leaves_buffer_untouched(gbr):
     buf = torch.zeros(trace.bytes_for(1), dtype=torch.uint8, device="cuda")
     src = torch.randn(1024, 512, device="cuda")
