@@ -554,7 +554,12 @@ def run_ours(args):
         with open(args.details, "w") as fh:
             json.dump({"other_workloads": others, "config4_as_written": config4,
                        "staged_copy": copy}, fh, indent=1)
-    peak_key = "bf16_tflops"
+    # Peak for the roofline: the burst cuBLAS figure for a short timed region,
+    # the sustained (power-capped) one once the region is long enough for the
+    # power cap to act (>= 100 ms) or the clock samples saw it acting.
+    long_run = t >= 0.1 or "sw_power_cap" in (clocks or {}).get("reasons", [])
+    peak_key = "bf16_tflops_sustained" if long_run and peaks.get("bf16_tflops_sustained") else "bf16_tflops"
+    other_key = "bf16_tflops" if peak_key != "bf16_tflops" else "bf16_tflops_sustained"
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 4),
@@ -571,10 +576,11 @@ def run_ours(args):
                      "peak": peaks.get(peak_key, FALLBACK_PEAKS[peak_key]), "unit": "TFLOP/s",
                      "frac": round(achieved / peaks.get(peak_key, FALLBACK_PEAKS[peak_key]), 4),
                      "traffic": recorded_traffic("gemm_umma_bf16"),
-                     "peak_source": "%s %s (burst cuBLAS bf16); sustained %s" % (
-                         peak_src, peak_key, peaks.get("bf16_tflops_sustained")),
-                     "frac_of_sustained": (round(achieved / peaks["bf16_tflops_sustained"], 4)
-                                           if peaks.get("bf16_tflops_sustained") else None)},
+                     "peak_source": "%s %s (%s cuBLAS bf16; timed region %.3f s)" % (
+                         peak_src, peak_key,
+                         "sustained" if peak_key.endswith("sustained") else "burst", t),
+                     "frac_of_" + ("burst" if other_key == "bf16_tflops" else "sustained"):
+                         (round(achieved / peaks[other_key], 4) if peaks.get(other_key) else None)},
         "e2e": {"value": round(flops * e2e_steps / t_e2e / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "steps": e2e_steps, "api": "gemm_bias_relu_host (C ABI, pinned host buffers)",
