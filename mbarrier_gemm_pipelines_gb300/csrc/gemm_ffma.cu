@@ -25,6 +25,10 @@
 // empty[s]: CW arrivals, one per consumer warp after its last read of the slot.
 // Slot/parity of k-iteration i (running across this CTA's tiles):
 //   slot = i % S, full parity = (i / S) & 1, empty parity = ((i / S) & 1) ^ 1.
+// A launch's last partial round of tiles can instead run as a split tail: the
+// whole tiles in one launch of this kernel, then a second, separate instance
+// (SPLIT) that deals the remaining tiles' k-blocks to every CTA and adds each
+// tile's parts in a fixed order (split_plan.cuh holds the schedule).
 #include "gbr_internal.h"
 #include "split_plan.cuh"
 
