@@ -25,6 +25,8 @@
 //     second 2-slot ring with the same slot/parity rule.
 //   * Epilogue: tcgen05.ld -> +bias -> ReLU -> (bf16 round-to-nearest-even)
 //     -> 128-byte swizzled st.shared -> TMA store, per warp, double-buffered.
+//     The tile's bias is staged in shared memory by one cp.async.bulk per
+//     tile (a one-slot ring of its own, bias_full / bias_empty).
 //   * Persistent CTAs walk tiles t = unit + j * units in banded order; every
 //     role walks the same sequence, and the k-iteration counter runs across
 //     tiles so phases carry over.
