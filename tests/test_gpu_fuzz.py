@@ -1,0 +1,157 @@
+"""Seeded random problems against the binary64 oracle, element by element.
+
+Each case draws its shape and every launch option at once: the kernel (FFMA in
+its three loaders, TF32, bf16), one CTA or a CTA pair per tile, one or two
+128-byte K slices per ring stage, the ring depth, the split tail (auto, never,
+forced), the dynamic tile counter and programmatic dependent launch.  M is any
+size from 1 row (a fifth of the draws take several rounds of tiles over the
+SMs), K may be 0, and N and K are multiples of 8 (the TMA row-pitch
+rule for bf16); half the draws make N a multiple of 64, where the B panels of a
+K slice come in one 3-D box, the rest take the per-panel boxes.  The grouped
+cases draw expert counts with empty and one-row experts the same way.  The
+draws come from a fixed seed, so a failing case id names a problem that can be
+rerun."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mbarrier_gemm_pipelines_gb300 import inputs
+from gpu_helpers import (TOL, load_library, rel_frobenius, require_gpu, split_tail, thin_tail,
+                         to_host_f64, tuned)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gbr():
+    require_gpu()
+    return load_library()
+
+
+class options:
+    """Sets the launch options of one case for a with-block, then restores the
+    defaults (automatic variant, auto split, static schedule, overlap on)."""
+
+    def __init__(self, gbr, pair, ks, split, dynamic, overlap):
+        self.gbr = gbr
+        self.ctx = [tuned(gbr, pair, ks), split_tail(gbr, split)]
+        self.dynamic, self.overlap = dynamic, overlap
+
+    def __enter__(self):
+        for c in self.ctx:
+            c.__enter__()
+        self.gbr.gemm_dynamic_schedule(self.dynamic)
+        self.gbr.launch_overlap(self.overlap)
+        return self
+
+    def __exit__(self, *exc):
+        self.gbr.launch_overlap(True)
+        self.gbr.gemm_dynamic_schedule(False)
+        for c in reversed(self.ctx):
+            c.__exit__(*exc)
+        return False
+
+
+def _stage_limit(dtype, pair, ks):
+    """Deepest ring each variant holds in shared memory (the library refuses
+    deeper ones with an error, which these draws stay clear of)."""
+    if dtype == "ffma_sync":
+        return 1
+    if dtype.startswith("ffma"):
+        return 4
+    if pair == 1:
+        return 4 if ks == 1 else 2
+    return 6 if ks == 1 else 3
+
+
+def _dense_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    kinds = ["ffma", "ffma_cpasync", "ffma_sync", "tf32", "tf32", "bf16", "bf16", "bf16"]
+    cases = []
+    for i in range(n):
+        dtype = kinds[rng.integers(len(kinds))]
+        M = int(rng.integers(1500, 5000)) if rng.random() < 0.2 else int(rng.integers(1, 1500))
+        N = 64 * int(rng.integers(1, 38)) if rng.random() < 0.5 else 8 * int(rng.integers(1, 300))
+        K = 0 if rng.random() < 0.05 else 8 * int(rng.integers(1, 260))
+        umma = dtype in ("tf32", "bf16")
+        pair = int(rng.choice([1, 2])) if umma else -1
+        ks = int(rng.choice([1, 2])) if umma else -1
+        S = int(rng.integers(1, _stage_limit(dtype, pair, ks) + 1))
+        split = int(rng.choice([-1, 0, 1]))
+        dynamic = bool(umma and rng.random() < 0.3)
+        overlap = bool(rng.random() < 0.7)
+        cases.append(pytest.param(dtype, M, N, K, pair, ks, S, split, dynamic, overlap,
+                                  id="d%02d-%s-%dx%dx%d-p%d-k%d-s%d-t%d-%s%s" % (
+                                      i, dtype, M, N, K, pair, ks, S, split,
+                                      "dyn" if dynamic else "st", "-ov" if overlap else "")))
+    return cases
+
+
+@pytest.mark.parametrize("dtype,M,N,K,pair,ks,S,split,dynamic,overlap", _dense_cases(96, 20261203))
+def test_dense_random(gbr, dtype, M, N, K, pair, ks, S, split, dynamic, overlap):
+    A, B, bias = inputs.gemm_normal(M, N, K, seed=M * 7 + N * 3 + K)
+    if dtype == "bf16":
+        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    with options(gbr, pair, ks, split, dynamic, overlap):
+        C = gbr.gemm_bias_relu(A.cuda(), B.cuda(), bias.cuda(), dtype=dtype, stages=S)
+    gbr.check_device()
+    got = to_host_f64(C)
+    ref = oracle.gemm_bias_relu(A.float(), B.float(), bias)
+    if dtype == "bf16":                    # the kernel rounds its output to bf16
+        ref_cmp = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+    else:
+        ref_cmp = ref
+    assert got.shape == (M, N)
+    assert (got >= 0).all()
+    if K == 0:
+        assert np.array_equal(got, ref_cmp)
+        return
+    assert rel_frobenius(got, ref) <= TOL[dtype]
+    scale = np.abs(ref).max() + 1e-30
+    assert np.abs(got - ref).max() <= 20 * TOL[dtype] * scale
+
+
+def _grouped_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        G = int(rng.integers(1, 10))
+        counts = []
+        for _ in range(G):
+            r = rng.random()
+            counts.append(0 if r < 0.15 else 1 if r < 0.25 else int(rng.integers(2, 700)))
+        K = 8 * int(rng.integers(1, 200))
+        N = 64 * int(rng.integers(1, 20)) if rng.random() < 0.5 else 8 * int(rng.integers(1, 160))
+        pair = int(rng.choice([-1, 1, 2]))
+        S = int(rng.integers(1, 5 if pair == 1 else 7))
+        split = int(rng.choice([-1, 0, 1]))
+        thin = bool(rng.random() < 0.7)
+        dynamic = bool(rng.random() < 0.3)
+        overlap = bool(rng.random() < 0.7)
+        cases.append(pytest.param(counts, K, N, pair, S, split, thin, dynamic, overlap,
+                                  id="g%02d-%s-%dx%d-p%d-s%d-t%d-%s-%s%s" % (
+                                      i, "_".join(map(str, counts)), K, N, pair, S, split,
+                                      "thin" if thin else "wide", "dyn" if dynamic else "st",
+                                      "-ov" if overlap else "")))
+    return cases
+
+
+@pytest.mark.parametrize("counts,K,N,pair,S,split,thin,dynamic,overlap",
+                         _grouped_cases(48, 31415))
+def test_grouped_random(gbr, counts, K, N, pair, S, split, thin, dynamic, overlap):
+    G, T = len(counts), sum(counts)
+    _, X, W, b = inputs.grouped(tokens=max(T, 1), experts=G, K=K, N=N, seed=T + K + N)
+    X = X[:T].contiguous()                 # all experts empty: a 0-row X
+    with options(gbr, pair, -1, split, dynamic, overlap), thin_tail(gbr, thin):
+        C = gbr.gemm_bias_relu_grouped(X.cuda(), W.cuda(), b.cuda(), counts, stages=S)
+    gbr.check_device()
+    got = to_host_f64(C)
+    assert got.shape == (T, N)
+    if T == 0:
+        return
+    ref = oracle.gemm_bias_relu_grouped(X.float(), W.float(), b, counts)
+    assert (got >= 0).all()
+    assert rel_frobenius(got, ref) <= TOL["bf16"]
+    scale = np.abs(ref).max() + 1e-30
+    assert np.abs(got - ref).max() <= 20 * TOL["bf16"] * scale
