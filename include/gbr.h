@@ -138,8 +138,10 @@ int gemm_bias_relu_grouped(const void *X, const void *W, const float *bias, void
  *   rows, cols  >= 0 and < 2^31; cols a multiple of 4.  Empty: nothing to do.
  *   tile_rows  1..256; tile_cols 4..256, a multiple of 4 (16-byte rows).
  *   stages  1 <= S <= gbr_max_stages(GBR_OP_COPY, 0, tile_rows, tile_cols),
- *         i.e. S * tile_rows * tile_cols * 4 bytes must fit in one CTA's
- *         shared memory (GBR_ERR_SMEM otherwise; at 128x64 fp32 S <= 7).
+ *         i.e. S slots of tile_rows * tile_cols * 4 bytes, each rounded up
+ *         to a multiple of 128 bytes (TMA's shared-memory alignment), must
+ *         fit in one CTA's shared memory (GBR_ERR_SMEM otherwise; at 128x64
+ *         fp32 S <= 7).
  */
 int staged_copy(const void *src, void *dst, int64_t rows, int64_t cols, int tile_rows,
                 int tile_cols, int stages, gbr_stream_t stream);

@@ -60,6 +60,11 @@ struct CopyArgs {
     FaultInjection inject;         // failure-detection self test only (zeroed: none)
 };
 
+// Distance between the staged copy's ring slots: the tile's bytes rounded up
+// to 128 (the alignment of a TMA copy's shared-memory address).
+__host__ __device__ constexpr uint32_t copy_slot_bytes(uint32_t tile_bytes) {
+    return (tile_bytes + 127u) & ~127u;
+}
 size_t copy_smem_bytes(int stages, uint32_t tile_bytes);
 cudaError_t copy_prepare(size_t smem);                 // per-device function attributes
 cudaError_t copy_occupancy(size_t smem, int* blocks_per_sm);

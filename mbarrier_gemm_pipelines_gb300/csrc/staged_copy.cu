@@ -13,6 +13,8 @@
 //                                              which counts as complete)
 // One lane of warp 0 loads, one lane of warp 1 stores.  CTAs are persistent:
 // CTA b copies tiles b, b + grid, b + 2 grid, ... so i is the CTA-local count.
+// Slots are copy_slot_bytes() apart: a TMA copy's shared-memory address must
+// be 128-byte aligned, and a tile may be any multiple of 16 bytes.
 #include "gbr_internal.h"
 
 namespace gbr {
@@ -25,7 +27,8 @@ __global__ void __launch_bounds__(64, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = align_1024(smem_raw);
     const int S = a.stages;
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + size_t(S) * a.tile_bytes);
+    const uint32_t slot_bytes = copy_slot_bytes(a.tile_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + size_t(S) * slot_bytes);
     uint64_t* empty = full + S;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
 
@@ -66,10 +69,10 @@ __global__ void __launch_bounds__(64, 1)
             trace_event(a.ctl, kRoleProducer, nt, kEvIssued, i, s, 0);   // before the load lands
             const int32_t tr = int32_t(t / a.tiles_c), tc = int32_t(t % a.tiles_c);
             if (hint_load)
-                ptx::tma_load_2d_hint(ring_base + s * a.tile_bytes, &src_map, fb, tc * a.tile_cols,
+                ptx::tma_load_2d_hint(ring_base + s * slot_bytes, &src_map, fb, tc * a.tile_cols,
                                       tr * a.tile_rows, ptx::l2_policy_evict_first());
             else
-                ptx::tma_load_2d(ring_base + s * a.tile_bytes, &src_map, fb, tc * a.tile_cols,
+                ptx::tma_load_2d(ring_base + s * slot_bytes, &src_map, fb, tc * a.tile_cols,
                                  tr * a.tile_rows);
         }
         trace_count(a.ctl, kRoleProducer, nt);
@@ -85,10 +88,10 @@ __global__ void __launch_bounds__(64, 1)
             trace_event(a.ctl, kRoleConsumer, nt, kEvWaitDone, i, s, ph);
             const int32_t tr = int32_t(t / a.tiles_c), tc = int32_t(t % a.tiles_c);
             if (hint_store)
-                ptx::tma_store_2d_hint(&dst_map, ring_base + s * a.tile_bytes, tc * a.tile_cols,
+                ptx::tma_store_2d_hint(&dst_map, ring_base + s * slot_bytes, tc * a.tile_cols,
                                        tr * a.tile_rows, ptx::l2_policy_evict_first());
             else
-                ptx::tma_store_2d(&dst_map, ring_base + s * a.tile_bytes, tc * a.tile_cols,
+                ptx::tma_store_2d(&dst_map, ring_base + s * slot_bytes, tc * a.tile_cols,
                                   tr * a.tile_rows);
             ptx::bulk_commit_group();
             if (a.store_lag == 0) {
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(64, 1)
 }  // namespace
 
 size_t copy_smem_bytes(int stages, uint32_t tile_bytes) {
-    return 1024 + size_t(stages) * tile_bytes + size_t(2 * stages) * 8 + 16;
+    return 1024 + size_t(stages) * copy_slot_bytes(tile_bytes) + size_t(2 * stages) * 8 + 16;
 }
 
 cudaError_t copy_prepare(size_t smem) {

@@ -44,6 +44,21 @@ def test_copy_small_bit_exact(gbr, rows, cols, tile, S):
     assert np.array_equal(_bits(dst), expect.view(np.int32))
 
 
+@pytest.mark.parametrize("tile,S", [((1, 8), 3), ((5, 12), 4), ((3, 4), 8), ((7, 36), 2),
+                                    ((1, 4), 1), ((33, 20), 5)])
+def test_copy_tiles_not_multiple_of_128_bytes(gbr, tile, S):
+    """Tiles of 16 to 3696 bytes that are not whole multiples of 128: every
+    ring slot still starts on a 128-byte boundary (TMA's shared-memory
+    alignment), and the copy is bit-exact."""
+    rows, cols = 1000, 612
+    src = inputs.uniform((rows, cols), -1e3, 1e3, inputs._gen(tile[0] * 131 + tile[1] + S))
+    expect = oracle.copy(src.numpy())
+    dst = torch.full((rows, cols), float("nan"), device="cuda")
+    gbr.staged_copy(src.cuda(), dst, tile=tile, stages=S)
+    gbr.check_device()
+    assert np.array_equal(_bits(dst), expect.view(np.int32))
+
+
 def test_copy_special_values(gbr):
     bits = np.array([0x7FC00001, 0x80000000, 0x7F800000, 0xFF800000, 0x00000001, 0x7F7FFFFF,
                      0xFFFFFFFF, 0x3F800000], dtype=np.uint32)

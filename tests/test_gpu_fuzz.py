@@ -5,12 +5,14 @@ its three loaders, TF32, bf16), one CTA or a CTA pair per tile, one or two
 128-byte K slices per ring stage, the ring depth, the split tail (auto, never,
 forced), the dynamic tile counter and programmatic dependent launch.  M is any
 size from 1 row (a fifth of the draws take several rounds of tiles over the
-SMs), K may be 0, and N and K are multiples of 8 (the TMA row-pitch
-rule for bf16); half the draws make N a multiple of 64, where the B panels of a
-K slice come in one 3-D box, the rest take the per-panel boxes.  The grouped
-cases draw expert counts with empty and one-row experts the same way.  The
-draws come from a fixed seed, so a failing case id names a problem that can be
-rerun."""
+SMs), K may be 0, and N and K are multiples of 16 bytes (the TMA row-pitch
+rule: 8 bf16 or 4 fp32 elements); half the draws make N a whole number of B
+panels (64 bf16 or 32 fp32 columns), where the panels of a K slice come in one
+3-D box, the rest take the per-panel boxes.  The grouped cases draw expert
+counts with empty and one-row experts the same way; the staged-copy cases draw
+shape, tile, ring depth and the copy's knobs; the host-buffer cases draw shape,
+kernel and pinned or pageable buffers.  The draws come from a fixed seed, so a
+failing case id names a problem that can be rerun."""
 import numpy as np
 import pytest
 import torch
@@ -71,9 +73,12 @@ def _dense_cases(n, seed):
     cases = []
     for i in range(n):
         dtype = kinds[rng.integers(len(kinds))]
+        q = 8 if dtype == "bf16" else 4                    # elements per 16 bytes
+        panel = 64 if dtype == "bf16" else 32
         M = int(rng.integers(1500, 5000)) if rng.random() < 0.2 else int(rng.integers(1, 1500))
-        N = 64 * int(rng.integers(1, 38)) if rng.random() < 0.5 else 8 * int(rng.integers(1, 300))
-        K = 0 if rng.random() < 0.05 else 8 * int(rng.integers(1, 260))
+        N = (panel * int(rng.integers(1, 2400 // panel)) if rng.random() < 0.5
+             else q * int(rng.integers(1, 2400 // q)))
+        K = 0 if rng.random() < 0.05 else q * int(rng.integers(1, 2080 // q))
         umma = dtype in ("tf32", "bf16")
         pair = int(rng.choice([1, 2])) if umma else -1
         ks = int(rng.choice([1, 2])) if umma else -1
@@ -155,3 +160,91 @@ def test_grouped_random(gbr, counts, K, N, pair, S, split, thin, dynamic, overla
     assert rel_frobenius(got, ref) <= TOL["bf16"]
     scale = np.abs(ref).max() + 1e-30
     assert np.abs(got - ref).max() <= 20 * TOL["bf16"] * scale
+
+
+def _copy_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        rows = 0 if rng.random() < 0.03 else int(rng.integers(1, 6000))
+        cols = 4 * int(rng.integers(1, 1100))
+        tr = int(rng.choice([1, 5, 8, 16, 32, 64, 100, 128, 256]))
+        tc = 4 * int(rng.choice([1, 2, 3, 8, 16, 24, 32, 64]))
+        dtype = "i32" if rng.random() < 0.3 else "f32"
+        lag = int(rng.choice([-1, 0, 1]))
+        hint = int(rng.choice([-1, 0, 1, 2, 3]))
+        ctas = int(rng.choice([-1, 1]))
+        u = rng.random()                                  # ring depth: a fraction of the limit
+        cases.append(pytest.param(rows, cols, tr, tc, dtype, lag, hint, ctas, u,
+                                  id="c%02d-%dx%d-t%dx%d-%s-l%d-h%d-c%d" % (
+                                      i, rows, cols, tr, tc, dtype, lag, hint, ctas)))
+    return cases
+
+
+@pytest.mark.parametrize("rows,cols,tr,tc,dtype,lag,hint,ctas,u", _copy_cases(40, 4242))
+def test_copy_random(gbr, rows, cols, tr, tc, dtype, lag, hint, ctas, u):
+    smax = min(gbr.max_stages(gbr.OP_COPY, 0, tr, tc), 8)
+    if smax == 0:                  # one tile does not fit a CTA's shared memory: rejected
+        with pytest.raises(gbr.GbrError) as e:
+            gbr.staged_copy(torch.zeros((8, 8), device="cuda"), tile=(tr, tc), stages=1)
+        assert e.value.code == 4   # GBR_ERR_SMEM
+        return
+    S = min(1 + int(u * smax), smax)
+    if lag == 1 and S < 2:
+        lag = 0
+    g = inputs._gen(rows * 31 + cols * 7 + tr + tc)
+    src = inputs.uniform((rows, cols), -1e3, 1e3, g)
+    if dtype == "i32":
+        src = src.view(torch.int32)
+    expect = oracle.copy(src.numpy())
+    dst = torch.full((rows, cols), -1, dtype=src.dtype, device="cuda")
+    gbr.copy_tuning(lag, ctas, hint)
+    try:
+        gbr.staged_copy(src.cuda(), dst, tile=(tr, tc), stages=S)
+        gbr.check_device()
+    finally:
+        gbr.copy_tuning(-1, -1, -1)
+    assert np.array_equal(dst.cpu().view(torch.int32).numpy(), expect.view(np.int32))
+
+
+def _host_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    kinds = ["ffma", "tf32", "bf16", "bf16"]
+    cases = []
+    for i in range(n):
+        dtype = kinds[rng.integers(len(kinds))]
+        q = 8 if dtype == "bf16" else 4
+        M = int(rng.integers(1, 5000))
+        N = q * int(rng.integers(1, 800 // q))
+        K = 0 if rng.random() < 0.1 else q * int(rng.integers(1, 800 // q))
+        S = int(rng.integers(1, 4))
+        pinned = bool(rng.random() < 0.7)
+        cases.append(pytest.param(dtype, M, N, K, S, pinned,
+                                  id="h%02d-%s-%dx%dx%d-s%d-%s" % (
+                                      i, dtype, M, N, K, S, "pin" if pinned else "page")))
+    return cases
+
+
+@pytest.mark.parametrize("dtype,M,N,K,S,pinned", _host_cases(16, 777))
+def test_host_random(gbr, dtype, M, N, K, S, pinned):
+    """gemm_bias_relu_host (copies in, GEMM in row chunks, copy out) against
+    the device-buffer call bit for bit (split tail off: both add every output's
+    products in the same order) and against the oracle."""
+    A, B, bias = inputs.gemm_normal(M, N, K, seed=M + 3 * N + 5 * K)
+    if dtype == "bf16":
+        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    if pinned:
+        A, B, bias = A.pin_memory(), B.pin_memory(), bias.pin_memory()
+    with split_tail(gbr, 0):
+        C = gbr.gemm_bias_relu_host(A, B, bias, dtype=dtype, stages=S)
+        D = gbr.gemm_bias_relu(A.cuda(), B.cuda(), bias.cuda(), dtype=dtype, stages=S)
+    gbr.check_device()
+    assert torch.equal(C, D.cpu())
+    got = to_host_f64(C)
+    ref = oracle.gemm_bias_relu(A.float(), B.float(), bias)
+    if K == 0:
+        if dtype == "bf16":
+            ref = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+        assert np.array_equal(got, ref)
+        return
+    assert rel_frobenius(got, ref) <= TOL[dtype]

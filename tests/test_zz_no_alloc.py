@@ -135,3 +135,29 @@ def test_noalloc_timeout_is_reported_then_cleared():
     gbr.gemm_bias_relu_tf32_noalloc(dA, dB, db, C, stages=3)
     gbr.check_device()
     _check_oracle(C, A, B, bias)
+
+
+def _noalloc_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        M = int(rng.integers(1, 3000))
+        N = 32 * int(rng.integers(1, 60)) if rng.random() < 0.5 else 4 * int(rng.integers(1, 500))
+        K = 4 * int(rng.integers(1, 500))
+        S = int(rng.integers(1, 5))
+        cases.append(pytest.param(M, N, K, S, id="n%02d-%dx%dx%d-s%d" % (i, M, N, K, S)))
+    return cases
+
+
+@pytest.mark.parametrize("M,N,K,S", _noalloc_cases(12, 9090))
+def test_noalloc_random(M, N, K, S):
+    """Seeded random shapes (N a whole number of 32-column B panels or only a
+    multiple of 4, every ring depth the call accepts) against the oracle."""
+    require_gpu()
+    gbr = load_library()
+    from mbarrier_gemm_pipelines_gb300 import _binding as b
+    A, B, bias = inputs.gemm_normal(M, N, K, seed=M + N + K + S)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    assert _noalloc(b.lib(), A.cuda(), B.cuda(), bias.cuda(), C, S) == b.OK, b.last_error()
+    gbr.check_device()
+    _check_oracle(C, A, B, bias)
