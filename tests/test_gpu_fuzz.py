@@ -248,3 +248,90 @@ def test_host_random(gbr, dtype, M, N, K, S, pinned):
         assert np.array_equal(got, ref)
         return
     assert rel_frobenius(got, ref) <= TOL[dtype]
+
+
+def _trace_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    kinds = ["copy", "ffma", "ffma_cpasync", "tf32", "bf16", "bf16", "grouped"]
+    cases = []
+    for i in range(n):
+        kind = kinds[rng.integers(len(kinds))]
+        pair = int(rng.choice([1, 2]))
+        ks = int(rng.choice([1, 2]))
+        split = int(rng.choice([-1, 0, 1]))
+        dyn = bool(kind in ("tf32", "bf16", "grouped") and rng.random() < 0.3)
+        q = 8 if kind in ("bf16", "grouped") else 4
+        M = int(rng.integers(1, 3000))
+        N = q * int(rng.integers(1, 2000 // q))
+        K = q * int(rng.integers(1, 1600 // q))
+        u = rng.random()
+        cases.append(pytest.param(kind, M, N, K, pair, ks, split, dyn, u,
+                                  id="t%02d-%s-%dx%dx%d-p%d-k%d-t%d-%s" % (
+                                      i, kind, M, N, K, pair, ks, split, "dyn" if dyn else "st")))
+    return cases
+
+
+@pytest.mark.parametrize("kind,M,N,K,pair,ks,split,dyn,u", _trace_cases(24, 5151))
+def test_trace_random(gbr, kind, M, N, K, pair, ks, split, dyn, u):
+    """Seeded random problems run by the traced kernel instances: the output
+    against the oracle, the recorded ring events through the protocol checker
+    and, unit by unit, through the oracle's ring-simulator replay."""
+    from mbarrier_gemm_pipelines_gb300 import trace
+    from test_gpu_trace import replay_units
+    from trace_check import check
+    if kind == "copy":
+        tr, tc = 8 * (1 + int(u * 16)), 4 * (1 + int(u * 32))     # up to 128 x 128
+        S = min(gbr.max_stages(gbr.OP_COPY, 0, tr, tc), 1 + int(u * 7))
+        src = inputs.uniform((M, 4 * (N // 4)), -1e3, 1e3, inputs._gen(M + N))
+        with trace.Recorder() as rec:
+            dst = gbr.staged_copy(src.cuda(), tile=(tr, tc), stages=S)
+            ev, cnt = rec.events()
+        gbr.check_device()
+        assert np.array_equal(dst.cpu().numpy(), oracle.copy(src.numpy()))
+        assert check(ev, cnt, S) == []
+        assert replay_units(ev, S) >= 1
+        return
+    if kind == "grouped":
+        G = 1 + int(u * 8)
+        counts = [int(c) for c in np.random.default_rng(M).integers(0, 2 * M // G + 2, G)]
+        _, X, W, b = inputs.grouped(tokens=max(sum(counts), 1), experts=G, K=K, N=N, seed=M + K)
+        X = X[:sum(counts)].contiguous()
+        S = 1 + int(u * (4 if pair == 1 else 3))
+        gbr.gemm_dynamic_schedule(dyn)
+        try:
+            with tuned(gbr, pair), split_tail(gbr, split), trace.Recorder() as rec:
+                C = gbr.gemm_bias_relu_grouped(X.cuda(), W.cuda(), b.cuda(), counts, stages=S)
+                ev, cnt = rec.events()
+        finally:
+            gbr.gemm_dynamic_schedule(False)
+        gbr.check_device()
+        if sum(counts) == 0:
+            return
+        ref = oracle.gemm_bias_relu_grouped(X.float(), W.float(), b, counts)
+        assert rel_frobenius(to_host_f64(C), ref) <= TOL["bf16"]
+        assert check(ev, cnt, S, cta_group=pair, accumulator=True) == []
+        assert replay_units(ev, S, cta_group=pair, accumulator=True) >= 1
+        return
+    A, B, bias = inputs.gemm_normal(M, N, K, seed=M + 2 * N + 3 * K)
+    if kind == "bf16":
+        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    umma = kind in ("tf32", "bf16")
+    S = 1 + int(u * ((4 if ks == 1 else 2) if pair == 1 else (6 if ks == 1 else 3))) if umma \
+        else 1 + int(u * 4)
+    gbr.gemm_dynamic_schedule(dyn)
+    try:
+        with tuned(gbr, pair if umma else -1, ks if umma else -1), split_tail(gbr, split):
+            with trace.Recorder() as rec:
+                C = gbr.gemm_bias_relu(A.cuda(), B.cuda(), bias.cuda(), dtype=kind, stages=S)
+                ev, cnt = rec.events()
+    finally:
+        gbr.gemm_dynamic_schedule(False)
+    gbr.check_device()
+    ref = oracle.gemm_bias_relu(A.float(), B.float(), bias)
+    assert rel_frobenius(to_host_f64(C), ref) <= TOL[kind]
+    if umma:
+        assert check(ev, cnt, S, cta_group=pair, accumulator=True) == []
+        assert replay_units(ev, S, cta_group=pair, accumulator=True) >= 1
+    else:
+        assert check(ev, cnt, S) == []
+        assert replay_units(ev, S) >= 1
