@@ -16,7 +16,8 @@ import torch
 
 import oracle
 from mbarrier_gemm_pipelines_gb300 import inputs
-from gpu_helpers import TOL, load_library, rel_frobenius, require_gpu, to_host_f64, tuned
+from gpu_helpers import (TOL, load_library, rel_frobenius, require_gpu, split_tail, to_host_f64,
+                         tuned)
 
 pytestmark = pytest.mark.gpu
 
@@ -177,3 +178,50 @@ def test_pair_repeated_injection_leaves_the_context_usable(gbr):
         _check_gemm(gbr, dA, dB, db, "bf16", 3)
     with tuned(gbr, 1):
         _check_gemm(gbr, dA, dB, db, "bf16", 4)
+
+
+def _random_injections(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        dtype = ["ffma", "bf16", "bf16", "tf32"][rng.integers(4)]
+        pair = int(rng.choice([1, 2])) if dtype != "ffma" else -1
+        ks = int(rng.choice([1, 2])) if dtype != "ffma" else -1
+        q = 8 if dtype == "bf16" else 4
+        M, N = int(rng.integers(1, 1200)), q * int(rng.integers(1, 1200 // q))
+        K = q * int(rng.integers(1, 1600 // q))
+        if dtype == "ffma":
+            S = int(rng.integers(1, 5))
+            tile_m, tile_n, kb = 128, 128, -(-K // 32)
+        else:
+            S = int(rng.integers(1, (4 if ks == 1 else 2) + 1 if pair == 1 else (6 if ks == 1 else 3) + 1))
+            tile_m, tile_n = 128 * pair, 256
+            kb = -(-K // ((64 if dtype == "bf16" else 32) * ks))
+        tiles = -(-M // tile_m) * -(-N // tile_n)
+        units = 152 if pair != 2 else 76
+        unit = int(rng.integers(0, min(tiles, units)))
+        item = int(rng.integers(0, kb))         # within the unit's first tile
+        cases.append(pytest.param(dtype, pair, ks, S, M, N, K, unit, item,
+                                  id="i%02d-%s-p%d-k%d-s%d-%dx%dx%d-u%d-j%d" % (
+                                      i, dtype, pair, ks, S, M, N, K, unit, item)))
+    return cases
+
+
+@pytest.mark.parametrize("dtype,pair,ks,S,M,N,K,unit,item", _random_injections(16, 8181))
+def test_random_unfilled_stage_times_out_and_recovers(gbr, dtype, pair, ks, S, M, N, K, unit, item):
+    """Seeded random shapes, variants, ring depths and injection points (a
+    unit that has a tile, an item within its first tile): the wait gives up,
+    the site is reported on one of the unit's CTAs, and a normal GEMM on the
+    same data afterwards matches the oracle."""
+    A, B, bias = inputs.gemm_uniform(M, N, K, seed=M + N + K)
+    dev_dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    dA, dB, db = A.to(dev_dt).cuda(), B.to(dev_dt).cuda(), bias.cuda()
+    with tuned(gbr, pair, ks), split_tail(gbr, 0):
+        gbr.selftest_gemm_skip_load(dA, dB, db, dtype, S, unit, item, LIMIT_NS)
+        code, msg = _status(gbr)
+        assert code == 6, msg
+        site, got_cta, got_item = _parse(msg)
+        cta_group = 2 if pair == 2 else 1
+        assert unit * cta_group <= got_cta < (unit + 1) * cta_group, (got_cta, unit)
+        assert gbr.device_status() == 0
+        _check_gemm(gbr, dA, dB, db, dtype, S)
