@@ -11,8 +11,10 @@ panels (64 bf16 or 32 fp32 columns), where the panels of a K slice come in one
 3-D box, the rest take the per-panel boxes.  The grouped cases draw expert
 counts with empty and one-row experts the same way; the staged-copy cases draw
 shape, tile, ring depth and the copy's knobs; the host-buffer cases draw shape,
-kernel and pinned or pageable buffers.  The draws come from a fixed seed, so a
-failing case id names a problem that can be rerun."""
+kernel and pinned or pageable buffers; the traced cases run the event-trace
+kernel instances and check their ring events as well as their outputs.  The
+draws come from fixed seeds, so a failing case id names a problem that can be
+rerun."""
 import numpy as np
 import pytest
 import torch
