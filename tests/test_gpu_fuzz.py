@@ -12,7 +12,8 @@ panels (64 bf16 or 32 fp32 columns), where the panels of a K slice come in one
 counts with empty and one-row experts the same way; the staged-copy cases draw
 shape, tile, ring depth and the copy's knobs; the host-buffer cases draw shape,
 kernel and pinned or pageable buffers; the traced cases run the event-trace
-kernel instances and check their ring events as well as their outputs.  The
+kernel instances and check their ring events as well as their outputs; the
+graph cases capture random call sequences into CUDA graphs and replay them.  The
 draws come from fixed seeds, so a failing case id names a problem that can be
 rerun."""
 import numpy as np
@@ -337,3 +338,101 @@ def test_trace_random(gbr, kind, M, N, K, pair, ks, split, dyn, u):
     else:
         assert check(ev, cnt, S) == []
         assert replay_units(ev, S) >= 1
+
+
+def _graph_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    return [pytest.param(int(rng.integers(0, 2 ** 31)), id="g%02d" % i) for i in range(n)]
+
+
+@pytest.mark.parametrize("case_seed", _graph_cases(12, 6262))
+def test_graph_random(gbr, case_seed):
+    """A random sequence of three calls (dense GEMM with a random kernel,
+    split mode and tile order; grouped GEMM; staged copy) captured into one
+    CUDA graph after an eager run, then replayed twice: each output matches
+    the oracle, and the eager output bit for bit where the call is
+    deterministic (every call but a tensor-core split tail, forced or chosen
+    by the automatic rule, whose parts are added in arrival order)."""
+    rng = np.random.default_rng(case_seed)
+    ops = []
+    for k in range(3):
+        kind = ["dense", "dense", "grouped", "copy"][rng.integers(4)]
+        if kind == "dense":
+            dtype = ["ffma", "tf32", "bf16"][rng.integers(3)]
+            q = 8 if dtype == "bf16" else 4
+            M, N, K = int(rng.integers(1, 2000)), q * int(rng.integers(1, 1200 // q)), \
+                q * int(rng.integers(1, 1600 // q))
+            split = int(rng.choice([-1, 0, 1]))
+            dyn = bool(dtype != "ffma" and rng.random() < 0.4)
+            A, B, bias = inputs.gemm_normal(M, N, K, seed=int(rng.integers(0, 10 ** 6)))
+            if dtype == "bf16":
+                A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+            dA, dB, db = A.cuda(), B.cuda(), bias.cuda()
+            C = torch.empty((M, N), dtype=dA.dtype, device="cuda")
+            ref = oracle.gemm_bias_relu(A.float(), B.float(), bias)
+
+            def call(st, dA=dA, dB=dB, db=db, C=C, dtype=dtype, split=split, dyn=dyn):
+                gbr.gemm_split_tail(split)
+                gbr.gemm_dynamic_schedule(dyn)
+                try:
+                    gbr.gemm_bias_relu(dA, dB, db, C, dtype=dtype, stages=3, stream=st)
+                finally:
+                    gbr.gemm_split_tail(-1)
+                    gbr.gemm_dynamic_schedule(False)
+            exact = dtype == "ffma" or dyn or split == 0    # no arrival-order split sums
+            ops.append((call, C, ref, TOL[dtype], exact))
+        elif kind == "grouped":
+            G = int(rng.integers(1, 6))
+            counts = [int(c) for c in rng.integers(0, 600, G)]
+            Kg, Ng = 8 * int(rng.integers(1, 100)), 8 * int(rng.integers(1, 100))
+            _, X, W, b = inputs.grouped(tokens=max(sum(counts), 1), experts=G, K=Kg, N=Ng,
+                                        seed=int(rng.integers(0, 10 ** 6)))
+            X = X[:sum(counts)].contiguous()
+            dX, dW, db = X.cuda(), W.cuda(), b.cuda()
+            Cg = torch.empty((sum(counts), Ng), dtype=torch.bfloat16, device="cuda")
+            ref = (oracle.gemm_bias_relu_grouped(X.float(), W.float(), b, counts)
+                   if sum(counts) else np.zeros((0, Ng)))
+
+            def call(st, dX=dX, dW=dW, db=db, counts=counts, Cg=Cg):
+                gbr.gemm_bias_relu_grouped(dX, dW, db, counts, Cg, stages=3, stream=st)
+            ops.append((call, Cg, ref, TOL["bf16"], True))
+        else:
+            rows, cols = int(rng.integers(1, 3000)), 4 * int(rng.integers(1, 600))
+            src = inputs.uniform((rows, cols), -1e3, 1e3, inputs._gen(rows + cols))
+            dsrc = src.cuda()
+            dst = torch.empty_like(dsrc)
+
+            def call(st, dsrc=dsrc, dst=dst):
+                gbr.staged_copy(dsrc, dst, tile=(64, 64), stages=4, stream=st)
+            ops.append((call, dst, src.numpy().astype(np.float64), 0.0, True))
+
+    def work():
+        st = torch.cuda.current_stream()
+        for call, *_ in ops:
+            call(st)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        work()                                  # eager run (also does per-device set-up)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    gbr.check_device()
+    eager = [out.clone() for _, out, *_ in ops]
+    for _, out, *_ in ops:
+        out.fill_(0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        work()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    gbr.check_device()
+    for (call, out, ref, tol, exact), e in zip(ops, eager):
+        got = to_host_f64(out)
+        if tol == 0.0:
+            assert np.array_equal(got, ref)
+        elif got.size:
+            assert rel_frobenius(got, ref) <= tol
+        if exact:
+            assert torch.equal(out, e)
